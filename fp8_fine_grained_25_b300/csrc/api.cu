@@ -1,0 +1,268 @@
+// The C ABI of libfp8q.so (declared in include/fp8q.h): argument checks,
+// device checks, TMA descriptor encoding and kernel launches. No device
+// memory is allocated here; every pointer belongs to the caller.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "fp8q.h"
+#include "gemm.cuh"
+#include "quant.cuh"
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct DeviceInfo {
+    bool init = false;
+    bool supported = false;
+    int sms = 0;
+};
+
+constexpr int kMaxDevices = 64;
+DeviceInfo g_devices[kMaxDevices];
+std::mutex g_mutex;
+uint64_t g_timeout_ns = 1000000000ull;
+int g_force_bn = 0;
+constexpr int64_t kI32Max = 2147483647;
+
+int current_device(DeviceInfo** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FP8Q_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return FP8Q_ERR_DEVICE;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceInfo& d = g_devices[dev];
+    if (!d.init) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return FP8Q_ERR_CUDA;
+        d.supported = (major == 10 && minor == 3);
+        d.sms = sms;
+        d.init = true;
+    }
+    if (!d.supported) return FP8Q_ERR_DEVICE;
+    *out = &d;
+    return FP8Q_OK;
+}
+
+EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// A row-major [outer, inner] tensor, boxes of [box_outer, box_inner]
+// elements, 128-byte swizzle, zero fill outside the tensor.
+bool make_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, uint64_t elem_bytes,
+                 const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                 uint32_t box_outer) {
+    EncodeTiledFn fn = encode_tiled();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {inner * elem_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t elem_strides[2] = {1, 1};
+    return fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, elem_strides,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Output-tile width: the one with the fewest tile-width units of work per
+// SM after rounding up to whole waves (a tile of width BN costs BN + 64
+// units: the fixed part is the 128-row A traffic and the per-tile epilogue).
+int choose_bn(int64_t M, int64_t N, int sms) {
+    int best = 256;
+    int64_t best_cost = -1;
+    for (int bn : {256, 128}) {
+        const int64_t tiles = cdiv(M, 128) * cdiv(N, bn);
+        const int64_t cost = cdiv(tiles, sms) * (bn + 64);
+        if (best_cost < 0 || cost < best_cost) {
+            best = bn;
+            best_cost = cost;
+        }
+    }
+    return best;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* fp8q_status_string(int status) {
+    switch (status) {
+        case FP8Q_OK: return "ok";
+        case FP8Q_ERR_NULL: return "a required pointer is NULL";
+        case FP8Q_ERR_SHAPE: return "invalid size (negative, zero, or too large)";
+        case FP8Q_ERR_ALIGN: return "K must be a multiple of 16, N of 8, and pointers 16-byte aligned";
+        case FP8Q_ERR_DEVICE: return "the current device is not sm_103 (B300)";
+        case FP8Q_ERR_CUDA: return "a CUDA call or kernel launch failed";
+        case FP8Q_ERR_TIMEOUT: return "a pipeline wait inside a kernel exceeded its time limit";
+        case FP8Q_ERR_UNSUPPORTED: return "unsupported request";
+        case FP8Q_ERR_OFFSETS: return "expert offsets are malformed";
+        default: return "unknown status";
+    }
+}
+
+void fp8q_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns = ns ? ns : 1000000000ull; }
+
+int fp8q_set_gemm_tile_n(int bn) {
+    if (bn != 0 && bn != 128 && bn != 256) return FP8Q_ERR_UNSUPPORTED;
+    g_force_bn = bn;
+    return FP8Q_OK;
+}
+
+int fp8q_get_device_status(cudaStream_t stream, uint32_t* status_out, int clear) {
+    if (!status_out) return FP8Q_ERR_NULL;
+    return fp8q::read_device_status(stream, status_out, clear != 0) == cudaSuccess ? FP8Q_OK
+                                                                                  : FP8Q_ERR_CUDA;
+}
+
+int fp8q_quant_act(const void* x_bf16, int64_t M, int64_t K, void* q_e4m3, float* scales,
+                   cudaStream_t stream) {
+    if (M < 0 || K <= 0 || M > kI32Max || K > kI32Max) return FP8Q_ERR_SHAPE;
+    if (M == 0) return FP8Q_OK;
+    if (!x_bf16 || !q_e4m3 || !scales) return FP8Q_ERR_NULL;
+    if (K % 16 != 0 || !aligned(x_bf16, 16) || !aligned(q_e4m3, 16) || !aligned(scales, 4))
+        return FP8Q_ERR_ALIGN;
+    if (M * cdiv(K, 128) > kI32Max) return FP8Q_ERR_SHAPE;
+    DeviceInfo* dev = nullptr;
+    if (int rc = current_device(&dev)) return rc;
+    return fp8q::launch_quant_act(x_bf16, M, K, q_e4m3, scales, stream, dev->sms) == cudaSuccess
+               ? FP8Q_OK
+               : FP8Q_ERR_CUDA;
+}
+
+int fp8q_quant_weight(const void* w_bf16, int64_t N, int64_t K, void* q_e4m3, float* scales,
+                      cudaStream_t stream) {
+    if (N < 0 || K <= 0 || N > kI32Max || K > kI32Max) return FP8Q_ERR_SHAPE;
+    if (N == 0) return FP8Q_OK;
+    if (!w_bf16 || !q_e4m3 || !scales) return FP8Q_ERR_NULL;
+    if (K % 16 != 0 || !aligned(w_bf16, 16) || !aligned(q_e4m3, 16) || !aligned(scales, 4))
+        return FP8Q_ERR_ALIGN;
+    DeviceInfo* dev = nullptr;
+    if (int rc = current_device(&dev)) return rc;
+    return fp8q::launch_quant_weight(w_bf16, N, K, q_e4m3, scales, stream, dev->sms) == cudaSuccess
+               ? FP8Q_OK
+               : FP8Q_ERR_CUDA;
+}
+
+int fp8_block_gemm(const void* A, const float* sa, const void* B, const float* sb, void* C_bf16,
+                   int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
+    if (M < 0 || N <= 0 || K <= 0 || M > kI32Max || N > kI32Max || K > kI32Max)
+        return FP8Q_ERR_SHAPE;
+    if (M == 0) return FP8Q_OK;
+    if (!A || !sa || !B || !sb || !C_bf16) return FP8Q_ERR_NULL;
+    if (K % 16 != 0 || N % 8 != 0 || !aligned(A, 16) || !aligned(B, 16) || !aligned(C_bf16, 16) ||
+        !aligned(sa, 4) || !aligned(sb, 4))
+        return FP8Q_ERR_ALIGN;
+    DeviceInfo* dev = nullptr;
+    if (int rc = current_device(&dev)) return rc;
+
+    const int bn = g_force_bn ? g_force_bn : choose_bn(M, N, dev->sms);
+    CUtensorMap tmA, tmB, tmC;
+    if (!make_map_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, K, M, 128, 128) ||
+        !make_map_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, K, N, 128, bn) ||
+        !make_map_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C_bf16, N, M, 64, 32))
+        return FP8Q_ERR_CUDA;
+
+    fp8q::GemmLaunch g{};
+    g.tmA = &tmA;
+    g.tmB = &tmB;
+    g.tmC = &tmC;
+    g.bn = bn;
+    g.grouped = false;
+    g.stream = stream;
+    fp8q::GemmArgs& a = g.args;
+    a.sa = sa;
+    a.sb = sb;
+    a.C = static_cast<__nv_bfloat16*>(C_bf16);
+    a.offsets = nullptr;
+    a.M = static_cast<int32_t>(M);
+    a.N = static_cast<int32_t>(N);
+    a.K = static_cast<int32_t>(K);
+    a.KB = static_cast<int32_t>(cdiv(K, 128));
+    a.NB = static_cast<int32_t>(cdiv(N, 128));
+    a.E = 1;
+    a.mt_count = static_cast<int32_t>(cdiv(M, 128));
+    a.nt_count = static_cast<int32_t>(cdiv(N, bn));
+    const int64_t tiles = static_cast<int64_t>(a.mt_count) * a.nt_count;
+    if (tiles > kI32Max) return FP8Q_ERR_SHAPE;
+    a.num_tiles = static_cast<int32_t>(tiles);
+    a.timeout_ns = g_timeout_ns;
+    a.debug = 0;
+    g.grid = static_cast<unsigned>(tiles < dev->sms ? tiles : dev->sms);
+    return fp8q::launch_gemm(g) == cudaSuccess ? FP8Q_OK : FP8Q_ERR_CUDA;
+}
+
+int fp8_grouped_gemm(const void* A, const float* sa, const void* B, const float* sb,
+                     void* C_bf16, const int32_t* expert_offsets, int32_t E, int64_t total_M,
+                     int64_t N, int64_t K, cudaStream_t stream) {
+    if (E < 1 || E > fp8q::kMaxExperts || total_M < 0 || N <= 0 || K <= 0 ||
+        total_M > kI32Max || N > kI32Max || K > kI32Max ||
+        static_cast<int64_t>(E) * N > kI32Max)
+        return FP8Q_ERR_SHAPE;
+    if (total_M == 0) return FP8Q_OK;
+    if (!A || !sa || !B || !sb || !C_bf16 || !expert_offsets) return FP8Q_ERR_NULL;
+    if (K % 16 != 0 || N % 8 != 0 || !aligned(A, 16) || !aligned(B, 16) || !aligned(C_bf16, 16) ||
+        !aligned(sa, 4) || !aligned(sb, 4) || !aligned(expert_offsets, 4))
+        return FP8Q_ERR_ALIGN;
+    DeviceInfo* dev = nullptr;
+    if (int rc = current_device(&dev)) return rc;
+
+    const int bn = 256;
+    CUtensorMap tmA, tmB;
+    if (!make_map_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, K, total_M, 128, 128) ||
+        !make_map_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, K, static_cast<uint64_t>(E) * N,
+                     128, bn))
+        return FP8Q_ERR_CUDA;
+
+    fp8q::GemmLaunch g{};
+    g.tmA = &tmA;
+    g.tmB = &tmB;
+    g.tmC = &tmA;  // unused: the grouped epilogue stores directly
+    g.bn = bn;
+    g.grouped = true;
+    g.stream = stream;
+    fp8q::GemmArgs& a = g.args;
+    a.sa = sa;
+    a.sb = sb;
+    a.C = static_cast<__nv_bfloat16*>(C_bf16);
+    a.offsets = expert_offsets;
+    a.M = static_cast<int32_t>(total_M);
+    a.N = static_cast<int32_t>(N);
+    a.K = static_cast<int32_t>(K);
+    a.KB = static_cast<int32_t>(cdiv(K, 128));
+    a.NB = static_cast<int32_t>(cdiv(N, 128));
+    a.E = E;
+    a.mt_count = 0;
+    a.nt_count = static_cast<int32_t>(cdiv(N, bn));
+    // Upper bound of the tile count (sum over experts of ceil(rows/128) *
+    // n-tiles) must fit the kernel's int32 tile ids.
+    if ((cdiv(total_M, 128) + E) * a.nt_count > kI32Max) return FP8Q_ERR_SHAPE;
+    a.num_tiles = 0;
+    a.timeout_ns = g_timeout_ns;
+    a.debug = 0;
+    g.grid = static_cast<unsigned>(dev->sms);
+    return fp8q::launch_gemm(g) == cudaSuccess ? FP8Q_OK : FP8Q_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,468 @@
+// Block-scaled FP8 GEMM on the sm_103a tensor cores, C = A * B^T, with the
+// fine-grained scales applied when each 128-wide K block's partial result is
+// promoted into FP32 registers (news.qq.com/rain/a/20241229A05OQF00,
+// "FP8 低精度训练": "细粒度量化" Fig. 7a for the scale granularity,
+// "提高累加精度" Fig. 7b for the promotion into FP32 registers).
+//
+// Per CTA (persistent, one 128 x BN output tile at a time):
+//   warp 0      TMA producer: per K block, a 128x128 A box and a BNx128 B box
+//               (E4M3, 128-byte swizzle) into a ring of shared-memory stages.
+//   warp 1      MMA issuer (one thread): 4 x tcgen05.mma kind::f8f6f4
+//               (K = 32 each) write P_kb = A_kb * B_kb^T into one of two TMEM
+//               buffers (fresh accumulate per K block), then commit to the
+//               stage's "empty" barrier and the buffer's "full" barrier.
+//               The same warp allocates and frees TMEM.
+//   warps 4-11  promotion + epilogue: tcgen05.ld P_kb (each warp owns 32
+//               TMEM lanes = 32 rows and half of the BN columns), then
+//               acc += P_kb * (sa[m][kb] * sb[n/128][kb]) in FP32 registers,
+//               release the TMEM buffer, and after the last K block convert
+//               to bf16 and store (TMA store for the dense GEMM, masked
+//               vector stores for the grouped one).
+// Double-buffered TMEM lets the MMA of K block kb+1 overlap the promotion of
+// block kb. Every wait is bounded in time; on expiry the CTA raises an
+// abort flag, drains its copies and MMAs, frees TMEM and returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "fp8q.h"
+#include "gemm.cuh"
+#include "ptx.cuh"
+
+namespace fp8q {
+
+__device__ uint32_t g_device_status;
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 128;
+constexpr int kThreads = 384;
+constexpr int kFirstEpiWarp = 4;
+constexpr int kEpiWarps = 8;
+constexpr int kGroupM = 16;  // rasterisation: m-tiles per group for L2 reuse
+constexpr int kSmemLimit = 232448;
+constexpr int kCtrlRegs = 40, kEpiRegs = 232;  // setmaxnreg split: 128*40 + 256*232 = 384*168
+
+template <int BN, bool GROUPED>
+struct Layout {
+    static constexpr int A_BYTES = BM * BK;
+    static constexpr int B_BYTES = BN * BK;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int EPI_WARP_BYTES = 32 * 64 * 2;  // 32 rows x 64 bf16 columns
+    static constexpr int EPI_BYTES = GROUPED ? 0 : kEpiWarps * EPI_WARP_BYTES;
+    static constexpr int RESERVE = 1024 /*alignment slack*/ + 256 /*barriers, flags*/ +
+                                   (GROUPED ? 4 * (kMaxExperts + 1) : 0);
+    static constexpr int STAGES_FIT = (kSmemLimit - RESERVE - EPI_BYTES) / STAGE_BYTES;
+    static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
+    static constexpr int EPI_OFF = STAGES * STAGE_BYTES;
+    static constexpr int BAR_OFF = EPI_OFF + EPI_BYTES;
+    // barriers: full[S], empty[S], tmem_full[2], tmem_empty[2], drain
+    static constexpr int NUM_BARS = 2 * STAGES + 5;
+    static constexpr int MISC_OFF = BAR_OFF + 8 * NUM_BARS;  // tmem slot, abort flag
+    static constexpr int TABLE_OFF = MISC_OFF + 16;
+    static constexpr int TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
+                                     : (2 * BN <= 256) ? 256 : 512;
+    static constexpr int HALF = BN / 2;  // columns per promotion warp
+    static constexpr int CHUNKS = HALF / 32;
+    static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN must be 64..256 in steps of 64");
+    static_assert(STAGES >= 2, "not enough shared memory for two stages");
+    static constexpr int smem_bytes(int E) {
+        return TABLE_OFF + (GROUPED ? 4 * (E + 1) : 0) + 1024;
+    }
+};
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+struct Tile {
+    int m0;       // first row of A / C
+    int row_end;  // rows >= row_end are not this tile's (expert end or M)
+    int n0;       // first column of C (= row of the expert's B)
+    int brow;     // B row coordinate in the 2-D B tensor ([E*N, K] when grouped)
+    int e;        // expert (0 when dense)
+};
+
+template <int BN, bool GROUPED>
+__device__ __forceinline__ Tile decode_tile(const GemmArgs& a, const int* table, int t) {
+    Tile r;
+    if constexpr (!GROUPED) {
+        const int per_group = kGroupM * a.nt_count;
+        const int g = t / per_group, in = t - g * per_group;
+        const int first = g * kGroupM;
+        const int gm = min(kGroupM, a.mt_count - first);
+        const int mt = first + in % gm, nt = in / gm;
+        r.m0 = mt * BM;
+        r.row_end = a.M;
+        r.n0 = nt * BN;
+        r.brow = r.n0;
+        r.e = 0;
+    } else {
+        int lo = 0, hi = a.E - 1;  // largest e with table[e] <= t
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (table[mid] <= t) lo = mid; else hi = mid - 1;
+        }
+        const int beg = __ldg(a.offsets + lo), end = __ldg(a.offsets + lo + 1);
+        const int mtiles = (end - beg + BM - 1) / BM;
+        const int local = t - table[lo];
+        const int nt = local / mtiles, mt = local - nt * mtiles;
+        r.m0 = beg + mt * BM;
+        r.row_end = end;
+        r.n0 = nt * BN;
+        r.brow = lo * a.N + r.n0;
+        r.e = lo;
+    }
+    return r;
+}
+
+// Grouped schedule, built by one warp: table[e] = number of tiles of experts
+// before e (m-tiles of ceil(rows/128) times n-tiles), table[E] = total.
+// Malformed offsets give total = 0 and set the device status.
+__device__ void build_group_table(const GemmArgs& a, int* table) {
+    const int lane = threadIdx.x & 31;
+    const int per = (a.E + 31) / 32;
+    const int b0 = min(a.E, lane * per), b1 = min(a.E, b0 + per);
+    bool bad = false;
+    int local = 0;
+    for (int e = b0; e < b1; ++e) {
+        const int lo = __ldg(a.offsets + e), hi = __ldg(a.offsets + e + 1);
+        if (hi < lo) bad = true;
+        else local += (hi - lo + BM - 1) / BM * a.nt_count;
+    }
+    if (lane == 0 && __ldg(a.offsets) != 0) bad = true;
+    if (lane == 31 && __ldg(a.offsets + a.E) != a.M) bad = true;
+    int incl = local;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int v = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+        if (lane >= d) incl += v;
+    }
+    int run = incl - local;
+    for (int e = b0; e < b1; ++e) {
+        table[e] = run;
+        const int lo = __ldg(a.offsets + e), hi = __ldg(a.offsets + e + 1);
+        if (hi >= lo) run += (hi - lo + BM - 1) / BM * a.nt_count;
+    }
+    const bool any_bad = __any_sync(0xFFFFFFFFu, bad);
+    const int total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    if (lane == 0) {
+        table[a.E] = any_bad ? 0 : total;
+        if (any_bad && blockIdx.x == 0) atomicOr(&g_device_status, FP8Q_DEVSTATUS_BAD_OFFSETS);
+    }
+}
+
+template <int BN, bool GROUPED>
+__global__ void __launch_bounds__(kThreads, 1)
+    fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
+    using L = Layout<BN, GROUPED>;
+    constexpr int S = L::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+    uint8_t* smem = smem_raw + pad;
+    const uint32_t sbase = raw + pad;
+
+    auto bar = [&](int i) -> uint32_t { return sbase + L::BAR_OFF + 8u * i; };
+    const int FULL = 0, EMPTY = S, TFULL = 2 * S, TEMPTY = 2 * S + 2, DRAIN = 2 * S + 4;
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + L::MISC_OFF);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::MISC_OFF + 4);
+    int* table = reinterpret_cast<int*>(smem + L::TABLE_OFF);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint64_t limit = args.timeout_ns;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(bar(FULL + s), 1);
+            mbar_init(bar(EMPTY + s), 1);
+        }
+        mbar_init(bar(TFULL + 0), 1);
+        mbar_init(bar(TFULL + 1), 1);
+        mbar_init(bar(TEMPTY + 0), kEpiWarps);
+        mbar_init(bar(TEMPTY + 1), kEpiWarps);
+        mbar_init(bar(DRAIN), 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+        if constexpr (!GROUPED) prefetch_tmap(&tmC);
+    }
+    if (warp == 1) {
+        tmem_alloc(sbase + L::MISC_OFF, L::TMEM_COLS);
+        tmem_relinquish_alloc_permit();
+    }
+    if constexpr (GROUPED) {
+        if (warp == 2) build_group_table(args, table);
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+    const int num_tiles = GROUPED ? table[args.E] : args.num_tiles;
+    const int KB = args.KB;
+
+    // Registers: 384 threads launch with 168 each (64512). The control
+    // warpgroup (producer, MMA, two idle warps) gives most of its share to
+    // the two promotion warpgroups, which hold a 128 x BN/2 FP32 accumulator
+    // slice (BN/2 registers per thread) plus a 32-column TMEM chunk:
+    // 128 * 40 + 256 * 232 = 64512.
+    if (warp < kFirstEpiWarp) setmaxnreg_dec<kCtrlRegs>();
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+                const Tile tile = decode_tile<BN, GROUPED>(args, table, t);
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(bar(EMPTY + stage), phase ^ 1u, abort_flag, limit)) {
+                        ok = false;
+                        break;
+                    }
+                    uint32_t bytes = L::STAGE_BYTES;
+                    if ((args.debug & 1u) && issued == 0) bytes += 16;  // never-completing phase
+                    mbar_arrive_expect_tx(bar(FULL + stage), bytes);
+                    const uint32_t sA = sbase + stage * L::STAGE_BYTES;
+                    tma_load_2d(sA, &tmA, bar(FULL + stage), kb * BK, tile.m0);
+                    tma_load_2d(sA + L::A_BYTES, &tmB, bar(FULL + stage), kb * BK, tile.brow);
+                    ++issued;
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // Wait for the copies still landing in shared memory (normally
+            // all consumed already) before the CTA may exit.
+            for (int s = 0; s < S; ++s) {
+                if (static_cast<uint32_t>(s) >= issued) break;
+                const uint32_t last = s + S * ((issued - 1 - s) / S);
+                volatile int local_flag = 0;
+                mbar_wait(bar(FULL + s), (last / S) & 1u, &local_flag, limit);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
+            int stage = 0;
+            uint32_t phase = 0, abuf = 0, aphase = 0;
+            bool ok = true, issued_any = false;
+            for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(bar(TEMPTY + abuf), aphase ^ 1u, abort_flag, limit) ||
+                        !mbar_wait(bar(FULL + stage), phase, abort_flag, limit)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t sA = sbase + stage * L::STAGE_BYTES;
+                    const uint64_t ad = sdesc_k_sw128(sA);
+                    const uint64_t bd = sdesc_k_sw128(sA + L::A_BYTES);
+                    const uint32_t d = tmem_base + abuf * BN;
+#pragma unroll
+                    for (int k = 0; k < BK / 32; ++k)
+                        mma_e4m3(d, ad + 2u * k, bd + 2u * k, idesc, k > 0 ? 1u : 0u);
+                    mma_commit(bar(EMPTY + stage));
+                    mma_commit(bar(TFULL + abuf));
+                    issued_any = true;
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                    abuf ^= 1u;
+                    if (abuf == 0) aphase ^= 1u;
+                }
+            }
+            // Every MMA issued above has completed once this arrives.
+            if (issued_any) {
+                mma_commit(bar(DRAIN));
+                volatile int local_flag = 0;
+                mbar_wait(bar(DRAIN), 0, &local_flag, limit);
+            }
+        }
+    } else if (warp >= kFirstEpiWarp) {
+        // ------------------------------------------- promotion + epilogue
+        setmaxnreg_inc<kEpiRegs>();
+        const int ew = warp - kFirstEpiWarp;  // 0..7
+        const int quarter = warp & 3;         // TMEM lanes 32*quarter .. +31
+        const int h = ew >> 2;                // column half
+        const int row = quarter * 32 + lane;  // row inside the tile
+        const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+        uint32_t abuf = 0, aphase = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+            const Tile tile = decode_tile<BN, GROUPED>(args, table, t);
+            const int m = tile.m0 + row;
+            const bool row_ok = m < tile.row_end;
+            const float* sa_row = args.sa + static_cast<int64_t>(row_ok ? m : 0) * KB;
+            const float* sb_e = args.sb + static_cast<int64_t>(tile.e) * args.NB * KB;
+            const int col0 = tile.n0 + h * L::HALF;  // first column of this warp
+            int nbk[L::CHUNKS];
+#pragma unroll
+            for (int c = 0; c < L::CHUNKS; ++c) {
+                const int nb = (col0 + 32 * c) >> 7;
+                nbk[c] = nb < args.NB ? nb * KB : -1;
+            }
+            float acc[L::HALF];
+#pragma unroll
+            for (int j = 0; j < L::HALF; ++j) acc[j] = 0.0f;
+
+            for (int kb = 0; kb < KB; ++kb) {
+                const float a_s = row_ok ? __ldg(sa_row + kb) : 0.0f;
+                float cs[L::CHUNKS];
+#pragma unroll
+                for (int c = 0; c < L::CHUNKS; ++c)
+                    cs[c] = nbk[c] >= 0 ? a_s * __ldg(sb_e + nbk[c] + kb) : 0.0f;
+                const bool got = mbar_wait(bar(TFULL + abuf), aphase, abort_flag, limit);
+                if (!__all_sync(0xFFFFFFFFu, got)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t taddr = lane_base + abuf * BN + h * L::HALF;
+#pragma unroll
+                for (int c = 0; c < L::CHUNKS; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(taddr + 32 * c, r);
+                    tmem_wait_ld32(r);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        acc[32 * c + j] = fmaf(__uint_as_float(r[j]), cs[c], acc[32 * c + j]);
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(TEMPTY + abuf));
+                abuf ^= 1u;
+                if (abuf == 0) aphase ^= 1u;
+            }
+            if (!ok) break;
+
+            if constexpr (!GROUPED) {
+                // bf16 -> swizzled staging (32 rows x 128 B per warp) -> TMA store
+                uint8_t* ebuf = smem + L::EPI_OFF + ew * L::EPI_WARP_BYTES;
+                const uint32_t ebuf_s = sbase + L::EPI_OFF + ew * L::EPI_WARP_BYTES;
+#pragma unroll
+                for (int c2 = 0; c2 < L::HALF / 64; ++c2) {
+                    if (lane == 0) bulk_wait_group_read0();
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const float* v = acc + 64 * c2 + 8 * j;
+                        uint4 pk;
+                        pk.x = pack_bf16x2(v[0], v[1]);
+                        pk.y = pack_bf16x2(v[2], v[3]);
+                        pk.z = pack_bf16x2(v[4], v[5]);
+                        pk.w = pack_bf16x2(v[6], v[7]);
+                        const int phys = j ^ (lane & 7);
+                        *reinterpret_cast<uint4*>(ebuf + lane * 128 + phys * 16) = pk;
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    const int x = col0 + 64 * c2, y = tile.m0 + quarter * 32;
+                    if (lane == 0 && x < args.N && y < args.M) {
+                        tma_store_2d(&tmC, ebuf_s, x, y);
+                        bulk_commit_group();
+                    }
+                }
+            } else {
+                // masked direct stores: rows past the expert's end belong to
+                // another expert's tile
+                if (row_ok) {
+                    __nv_bfloat16* crow = args.C + static_cast<int64_t>(m) * args.N;
+#pragma unroll
+                    for (int j = 0; j < L::HALF / 8; ++j) {
+                        const int col = col0 + 8 * j;
+                        if (col < args.N) {
+                            const float* v = acc + 8 * j;
+                            uint4 pk;
+                            pk.x = pack_bf16x2(v[0], v[1]);
+                            pk.y = pack_bf16x2(v[2], v[3]);
+                            pk.z = pack_bf16x2(v[4], v[5]);
+                            pk.w = pack_bf16x2(v[6], v[7]);
+                            *reinterpret_cast<uint4*>(crow + col) = pk;
+                        }
+                    }
+                }
+            }
+        }
+        if constexpr (!GROUPED) {
+            if (lane == 0) bulk_wait_group0();
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, L::TMEM_COLS);
+    }
+    if (threadIdx.x == 0 && *abort_flag) atomicOr(&g_device_status, FP8Q_DEVSTATUS_TIMEOUT);
+}
+
+template <int BN, bool GROUPED>
+cudaError_t launch_one(const GemmLaunch& g) {
+    using L = Layout<BN, GROUPED>;
+    auto kern = fp8_gemm_kernel<BN, GROUPED>;
+    // setmaxnreg.inc waits until the registers it asks for are free in the
+    // CTA's launch pool; a pool smaller than the split would never satisfy
+    // it, so refuse to launch in that case.
+    cudaFuncAttributes fa;
+    cudaError_t err = cudaFuncGetAttributes(&fa, kern);
+    if (err != cudaSuccess) return err;
+    if (fa.numRegs * kThreads < kCtrlRegs * 128 + kEpiRegs * 256 || fa.maxThreadsPerBlock < kThreads)
+        return cudaErrorInvalidConfiguration;
+    const int smem = L::smem_bytes(GROUPED ? g.args.E : 0);
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+    kern<<<g.grid, kThreads, smem, g.stream>>>(*g.tmA, *g.tmB, *g.tmC, g.args);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int gemm_stages(int bn) {
+    switch (bn) {
+        case 128: return Layout<128, false>::STAGES;
+        case 256: return Layout<256, false>::STAGES;
+        default: return 0;
+    }
+}
+
+cudaError_t launch_gemm(const GemmLaunch& g) {
+    if (g.grouped) {
+        switch (g.bn) {
+            case 128: return launch_one<128, true>(g);
+            case 256: return launch_one<256, true>(g);
+        }
+    } else {
+        switch (g.bn) {
+            case 128: return launch_one<128, false>(g);
+            case 256: return launch_one<256, false>(g);
+        }
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t read_device_status(cudaStream_t stream, uint32_t* out, bool clear) {
+    cudaError_t err = cudaStreamSynchronize(stream);
+    if (err != cudaSuccess) return err;
+    err = cudaMemcpyFromSymbol(out, g_device_status, sizeof(uint32_t));
+    if (err != cudaSuccess || !clear) return err;
+    const uint32_t zero = 0;
+    return cudaMemcpyToSymbol(g_device_status, &zero, sizeof(uint32_t));
+}
+
+}  // namespace fp8q

@@ -1,0 +1,42 @@
+// Internal interface between the C-ABI layer and the GEMM kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fp8q {
+
+constexpr int kMaxExperts = 1024;
+
+struct GemmArgs {
+    const float* sa;         // [M, KB]
+    const float* sb;         // [NB, KB], or [E][NB][KB] when grouped
+    __nv_bfloat16* C;        // [M, N] (written directly by the grouped epilogue)
+    const int32_t* offsets;  // [E + 1], grouped only (device memory)
+    int32_t M, N, K;         // M = total rows of A and C
+    int32_t KB, NB;          // ceil(K / 128), ceil(N / 128)
+    int32_t E;               // experts (grouped), else 1
+    int32_t mt_count, nt_count;
+    int32_t num_tiles;       // dense only; the grouped kernel counts its own
+    uint64_t timeout_ns;
+    uint32_t debug;          // bit 0: make the first pipeline stage never complete
+};
+
+struct GemmLaunch {
+    const CUtensorMap* tmA;
+    const CUtensorMap* tmB;
+    const CUtensorMap* tmC;
+    GemmArgs args;
+    int bn;
+    bool grouped;
+    unsigned grid;
+    cudaStream_t stream;
+};
+
+cudaError_t launch_gemm(const GemmLaunch& g);
+int gemm_stages(int bn);
+cudaError_t read_device_status(cudaStream_t stream, uint32_t* out, bool clear);
+
+}  // namespace fp8q

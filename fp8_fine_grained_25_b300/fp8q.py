@@ -1,0 +1,183 @@
+"""Python binding of libfp8q.so: the C-ABI entry points of include/fp8q.h
+under the same names, taking torch CUDA tensors.
+
+This module only marshals arguments (shapes, pointers, the current CUDA
+stream) and, where an output is not given, allocates it with torch. Every
+step of the computation runs in the library's CUDA kernels; there is no
+other implementation behind these names. Importing this module fails if
+the library has not been built (``python -m fp8_fine_grained_25_b300.build``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfp8q.so")
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(f"{_LIB_PATH} is missing: build it with "
+                      "`python -m fp8_fine_grained_25_b300.build` (nvcc, sm_103a)")
+
+lib = ctypes.CDLL(_LIB_PATH)
+_i64, _i32, _p = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p
+lib.fp8q_quant_act.argtypes = [_p, _i64, _i64, _p, _p, _p]
+lib.fp8q_quant_weight.argtypes = [_p, _i64, _i64, _p, _p, _p]
+lib.fp8_block_gemm.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p]
+lib.fp8_grouped_gemm.argtypes = [_p, _p, _p, _p, _p, _p, _i32, _i64, _i64, _i64, _p]
+lib.fp8q_get_device_status.argtypes = [_p, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
+lib.fp8q_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
+lib.fp8q_set_wait_timeout_ns.restype = None
+lib.fp8q_set_gemm_tile_n.argtypes = [ctypes.c_int]
+lib.fp8q_set_gemm_tile_n.restype = ctypes.c_int
+lib.fp8q_status_string.argtypes = [ctypes.c_int]
+lib.fp8q_status_string.restype = ctypes.c_char_p
+for _f in ("fp8q_quant_act", "fp8q_quant_weight", "fp8_block_gemm", "fp8_grouped_gemm",
+           "fp8q_get_device_status"):
+    getattr(lib, _f).restype = ctypes.c_int
+
+OK, ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_DEVICE, ERR_CUDA, ERR_TIMEOUT, ERR_UNSUPPORTED, ERR_OFFSETS = range(9)
+DEVSTATUS_TIMEOUT = 0x1
+DEVSTATUS_BAD_OFFSETS = 0x2
+
+CODE_DTYPES = (torch.uint8, torch.float8_e4m3fn)
+
+
+class FP8QError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {fp8q_status_string(status)} (status {status})")
+
+
+def fp8q_status_string(status: int) -> str:
+    return lib.fp8q_status_string(int(status)).decode()
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != OK:
+        raise FP8QError(rc, where)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _need(t: torch.Tensor, name: str, dtypes, shape) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name}: dtype {t.dtype} not in {dtypes}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)} != {tuple(shape)}")
+
+
+def _cdiv(a: int, b: int) -> int:
+    return -(-a // b)
+
+
+def fp8q_quant_act(x: torch.Tensor, q: torch.Tensor | None = None,
+                   scales: torch.Tensor | None = None, stream=None):
+    """1x128-tile quantization of bf16 activations x [M, K] -> (q uint8 [M, K],
+    scales fp32 [M, ceil(K/128)])."""
+    M, K = x.shape
+    _need(x, "x", (torch.bfloat16,), None)
+    if q is None:
+        q = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty((M, _cdiv(K, 128)), dtype=torch.float32, device=x.device)
+    _need(q, "q", CODE_DTYPES, (M, K))
+    _need(scales, "scales", (torch.float32,), (M, _cdiv(K, 128)))
+    _check(lib.fp8q_quant_act(x.data_ptr(), M, K, q.data_ptr(), scales.data_ptr(), _stream(stream)),
+           "fp8q_quant_act")
+    return q, scales
+
+
+def fp8q_quant_weight(w: torch.Tensor, q: torch.Tensor | None = None,
+                      scales: torch.Tensor | None = None, stream=None):
+    """128x128-block quantization of bf16 weights w [N, K] (or a stack
+    [E, N, K] with N % 128 == 0) -> (q uint8, scales fp32 [.., ceil(N/128), ceil(K/128)])."""
+    _need(w, "w", (torch.bfloat16,), None)
+    shape = tuple(w.shape)
+    if len(shape) == 3:
+        E, N, K = shape
+        if N % 128:
+            raise ValueError("a weight stack needs N % 128 == 0")
+        rows, sshape = E * N, (E, N // 128, _cdiv(K, 128))
+    else:
+        N, K = shape
+        rows, sshape = N, (_cdiv(N, 128), _cdiv(K, 128))
+    if q is None:
+        q = torch.empty(shape, dtype=torch.uint8, device=w.device)
+    if scales is None:
+        scales = torch.empty(sshape, dtype=torch.float32, device=w.device)
+    _need(q, "q", CODE_DTYPES, shape)
+    _need(scales, "scales", (torch.float32,), sshape)
+    _check(lib.fp8q_quant_weight(w.data_ptr(), rows, K, q.data_ptr(), scales.data_ptr(),
+                                 _stream(stream)), "fp8q_quant_weight")
+    return q, scales
+
+
+def fp8_block_gemm(A: torch.Tensor, sa: torch.Tensor, B: torch.Tensor, sb: torch.Tensor,
+                   C: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """C[M, N] (bf16) = block-scaled A[M, K] * B[N, K]^T."""
+    M, K = A.shape
+    N = B.shape[0]
+    _need(A, "A", CODE_DTYPES, (M, K))
+    _need(B, "B", CODE_DTYPES, (N, K))
+    _need(sa, "sa", (torch.float32,), (M, _cdiv(K, 128)))
+    _need(sb, "sb", (torch.float32,), (_cdiv(N, 128), _cdiv(K, 128)))
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    _need(C, "C", (torch.bfloat16,), (M, N))
+    _check(lib.fp8_block_gemm(A.data_ptr(), sa.data_ptr(), B.data_ptr(), sb.data_ptr(),
+                              C.data_ptr(), M, N, K, _stream(stream)), "fp8_block_gemm")
+    return C
+
+
+def fp8_grouped_gemm(A: torch.Tensor, sa: torch.Tensor, B: torch.Tensor, sb: torch.Tensor,
+                     expert_offsets: torch.Tensor, C: torch.Tensor | None = None,
+                     total_M: int | None = None, stream=None) -> torch.Tensor:
+    """Grouped GEMM: rows [off[e], off[e+1]) of A use expert e of B [E, N, K].
+
+    ``total_M`` defaults to A.shape[0] (the offsets stay on the device)."""
+    M, K = A.shape
+    E, N, Kb = B.shape
+    if Kb != K:
+        raise ValueError("A and B disagree on K")
+    total_M = M if total_M is None else int(total_M)
+    _need(A, "A", CODE_DTYPES, (M, K))
+    _need(B, "B", CODE_DTYPES, (E, N, K))
+    _need(sa, "sa", (torch.float32,), (M, _cdiv(K, 128)))
+    _need(sb, "sb", (torch.float32,), (E, _cdiv(N, 128), _cdiv(K, 128)))
+    _need(expert_offsets, "expert_offsets", (torch.int32,), (E + 1,))
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    _need(C, "C", (torch.bfloat16,), (M, N))
+    _check(lib.fp8_grouped_gemm(A.data_ptr(), sa.data_ptr(), B.data_ptr(), sb.data_ptr(),
+                                C.data_ptr(), expert_offsets.data_ptr(), E, total_M, N, K,
+                                _stream(stream)), "fp8_grouped_gemm")
+    return C
+
+
+def fp8q_get_device_status(stream=None, clear: bool = True) -> int:
+    """Synchronize the stream and return (and by default clear) the device
+    status word (DEVSTATUS_* bits)."""
+    out = ctypes.c_uint32(0)
+    _check(lib.fp8q_get_device_status(_stream(stream), ctypes.byref(out), int(bool(clear))),
+           "fp8q_get_device_status")
+    return out.value
+
+
+def fp8q_set_wait_timeout_ns(ns: int) -> None:
+    lib.fp8q_set_wait_timeout_ns(int(ns))
+
+
+def fp8q_set_gemm_tile_n(bn: int) -> None:
+    """Force the dense GEMM's output-tile width (128 or 256; 0 = automatic)."""
+    _check(lib.fp8q_set_gemm_tile_n(int(bn)), "fp8q_set_gemm_tile_n")

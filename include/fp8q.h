@@ -1,0 +1,161 @@
+/*
+ * fp8q: fine-grained FP8 quantization and block-scaled FP8 GEMM for B300
+ * (sm_103a), behind a plain C ABI.
+ *
+ * What the method computes (extracted web pages on DeepSeek-V3 training):
+ *  - news.qq.com/rain/a/20241229A05OQF00, section "FP8 低精度训练",
+ *    item "细粒度量化" (Fig. 7a): activations get one scale per 1x128 tile
+ *    (per token, per 128 channels), weights one scale per 128x128 block.
+ *  - same section, item "提高累加精度" (Fig. 7b): the FP8 MMA partial results
+ *    are promoted into FP32 registers, which is where the fine-grained
+ *    scales are applied.
+ *  - developer.aliyun.com/article/1776647 §4.1 and m.jxzklqfsx.com/aigc/3586
+ *    §三(二): block-wise quantization plus high-precision accumulation.
+ * The pages name neither the FP8 encoding nor the scale formula. This
+ * library uses E4M3 (OCP E4M3FN, max 448), scale = fl32(amax / 448), codes
+ * q = E4M3_round_nearest_even_saturating(fl32(x / scale)), and an all-zero
+ * tile gets scale 0 and all-zero codes.
+ *
+ * Conventions for every entry point:
+ *  - Pointers are DEVICE pointers on the current CUDA device, owned by the
+ *    caller, and must be 16-byte aligned. The library allocates no device
+ *    memory and keeps no reference to a pointer after the call returns.
+ *  - Matrices are dense and row-major with unit inner stride. FP8 codes are
+ *    one byte each (E4M3 bit patterns); bf16 values are raw 16-bit patterns.
+ *  - K must be a multiple of 16 (the FP8 row pitch must be a multiple of 16
+ *    bytes) and N a multiple of 8 (the bf16 output row pitch likewise);
+ *    otherwise the call returns FP8Q_ERR_ALIGN. M = 0 (or total_M = 0) is a
+ *    no-op that returns FP8Q_OK. Sizes above 2^31 - 1 rows or columns give
+ *    FP8Q_ERR_SHAPE.
+ *  - Work is enqueued on `stream` and runs asynchronously. Argument checks
+ *    happen before anything is enqueued; a failed check enqueues nothing.
+ *    A launch failure returns FP8Q_ERR_CUDA.
+ *  - Inputs must be finite; NaN or Inf input gives undefined codes.
+ *  - Only sm_103 devices are supported (FP8Q_ERR_DEVICE otherwise).
+ *  - Kernel-side failures (a pipeline wait that exceeds its time limit, or
+ *    malformed expert offsets) set a device status word that
+ *    fp8q_get_device_status() reads; the kernel then returns early.
+ */
+#ifndef FP8Q_H
+#define FP8Q_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define FP8Q_API __attribute__((visibility("default")))
+#else
+#define FP8Q_API
+#endif
+
+#if !defined(__DRIVER_TYPES_H__)
+typedef struct CUstream_st* cudaStream_t; /* the CUDA runtime's stream handle */
+#endif
+
+typedef enum {
+    FP8Q_OK = 0,
+    FP8Q_ERR_NULL = 1,        /* a required pointer is NULL */
+    FP8Q_ERR_SHAPE = 2,       /* a size is negative, zero where not allowed, or too large */
+    FP8Q_ERR_ALIGN = 3,       /* K % 16 != 0, N % 8 != 0, or a pointer not 16-byte aligned */
+    FP8Q_ERR_DEVICE = 4,      /* the current device is not sm_103 */
+    FP8Q_ERR_CUDA = 5,        /* a CUDA runtime/driver call or a launch failed */
+    FP8Q_ERR_TIMEOUT = 6,     /* device status: a pipeline wait exceeded its limit */
+    FP8Q_ERR_UNSUPPORTED = 7, /* a valid request this build does not handle */
+    FP8Q_ERR_OFFSETS = 8      /* device status: expert offsets malformed */
+} fp8q_status;
+
+/* Device status word bits (see fp8q_get_device_status). */
+#define FP8Q_DEVSTATUS_TIMEOUT 0x1u
+#define FP8Q_DEVSTATUS_BAD_OFFSETS 0x2u
+
+/*
+ * Activation quantization, one scale per 1x128 tile (Fig. 7a, "1x128
+ * tile-wise").
+ *   x_bf16  in : bf16 [M, K]
+ *   q_e4m3  out: uint8 E4M3 codes [M, K]
+ *   scales  out: fp32 [M, ceil(K/128)]; scales[m][kb] = amax(|x[m, 128kb ..
+ *                128kb+127]|) / 448, over the present columns when K % 128 != 0.
+ * Codes and scales are bit-exact with the definition above.
+ */
+FP8Q_API int fp8q_quant_act(const void* x_bf16, int64_t M, int64_t K, void* q_e4m3, float* scales,
+                   cudaStream_t stream);
+
+/*
+ * Weight quantization, one scale per 128x128 block (Fig. 7a, "128x128
+ * block-wise"; aliyun §4.1 "块级量化（128×128 块）").
+ *   w_bf16  in : bf16 [N, K]
+ *   q_e4m3  out: uint8 E4M3 codes [N, K]
+ *   scales  out: fp32 [ceil(N/128), ceil(K/128)]; the amax runs over the block's
+ *                present rows and columns at the N and K tails.
+ * A stack of E expert weights [E][N][K] with N % 128 == 0 is quantized in one
+ * call as an [E*N, K] matrix; its scales come out as [E][N/128][ceil(K/128)].
+ */
+FP8Q_API int fp8q_quant_weight(const void* w_bf16, int64_t N, int64_t K, void* q_e4m3, float* scales,
+                      cudaStream_t stream);
+
+/*
+ * Block-scaled FP8 GEMM, C = A * B^T (Fig. 7b: FP8 MMA per 128-wide K block,
+ * promoted to FP32 with the fine-grained scales).
+ *   A  in : E4M3 codes [M, K]        sa in: fp32 [M, ceil(K/128)]
+ *   B  in : E4M3 codes [N, K]        sb in: fp32 [ceil(N/128), ceil(K/128)]
+ *   C  out: bf16 [M, N]
+ *   C[m][n] = bf16_rn( sum_kb  P_kb[m][n] * (sa[m][kb] * sb[n/128][kb]) ),
+ *   P_kb = sum over k in block kb of dec(A[m][k]) * dec(B[n][k]), taken on the
+ *   tensor cores with FP32 accumulation; the sum over kb runs in FP32.
+ * Accuracy: |C - exact-definition-in-FP32| <= 1 bf16 ulp + 1e-5 * sum_k|a_k b_k|.
+ */
+FP8Q_API int fp8_block_gemm(const void* A, const float* sa, const void* B, const float* sb, void* C_bf16,
+                   int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+
+/*
+ * Grouped (per-expert) block-scaled FP8 GEMM for the MoE FFN (news.qq.com
+ * page, "DeepSeekMoE 架构": 256 routed experts, 8 per token). Rows of A are
+ * grouped by expert: rows [off[e], off[e+1]) use expert e's weights.
+ *   A   in : E4M3 codes [total_M, K]      sa in: fp32 [total_M, ceil(K/128)]
+ *   B   in : E4M3 codes [E][N][K]         sb in: fp32 [E][ceil(N/128)][ceil(K/128)]
+ *   C   out: bf16 [total_M, N]; row m = A[m] * B_e^T for its expert e
+ *   expert_offsets in: DEVICE int32 [E+1], off[0] = 0, nondecreasing,
+ *                      off[E] = total_M (empty experts allowed)
+ *   E: 1 .. 1024; total_M: passed from the host (= off[E]).
+ * The host never reads the offsets. Malformed offsets (decreasing, off[0] != 0
+ * or off[E] != total_M) are detected on the device: nothing is written to C
+ * and the device status word gets FP8Q_DEVSTATUS_BAD_OFFSETS.
+ */
+FP8Q_API int fp8_grouped_gemm(const void* A, const float* sa, const void* B, const float* sb,
+                     void* C_bf16, const int32_t* expert_offsets, int32_t E, int64_t total_M,
+                     int64_t N, int64_t K, cudaStream_t stream);
+
+/*
+ * Synchronizes `stream`, then reads the device status word (an OR of
+ * FP8Q_DEVSTATUS_* bits set by kernels since the last clear) of the current
+ * device into *status_out, and clears it when `clear` is nonzero.
+ * Returns FP8Q_OK, FP8Q_ERR_NULL or FP8Q_ERR_CUDA.
+ */
+FP8Q_API int fp8q_get_device_status(cudaStream_t stream, uint32_t* status_out, int clear);
+
+/*
+ * Time limit for every pipeline wait inside the GEMM kernels, in
+ * nanoseconds (default 1e9). A wait that exceeds it sets
+ * FP8Q_DEVSTATUS_TIMEOUT, and the kernel drains its in-flight copies,
+ * frees its tensor memory and returns. 0 restores the default.
+ */
+FP8Q_API void fp8q_set_wait_timeout_ns(uint64_t ns);
+
+/*
+ * Output-tile width of fp8_block_gemm: 128 or 256 columns, or 0 (the
+ * default) to let the library pick per shape. Affects speed only, never
+ * results. Returns FP8Q_ERR_UNSUPPORTED for other values.
+ */
+FP8Q_API int fp8q_set_gemm_tile_n(int bn);
+
+/* A short English description of a status code. Never NULL. */
+FP8Q_API const char* fp8q_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8Q_H */

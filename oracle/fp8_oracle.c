@@ -208,9 +208,9 @@ void fp8o_block_partials(const uint8_t* qa, const uint8_t* qb, int64_t K, int64_
  * the acceptance bound.
  *   qa [M, K], sa [M, KB]; qb [N, K], sb [ceil(N/128), KB]; row-major.
  */
-static void gemm_element(const uint8_t* qa, const float* sa, const uint8_t* qb,
-                         const float* sb, int64_t K, int64_t m, int64_t n, float* c32,
-                         double* S) {
+static void gemm_element(const double* dec, const uint8_t* qa, const float* sa,
+                         const uint8_t* qb, const float* sb, int64_t K, int64_t m, int64_t n,
+                         float* c32, double* S) {
     int64_t KB = (K + TILE - 1) / TILE;
     float acc = 0.0f;
     double bound = 0.0;
@@ -219,7 +219,7 @@ static void gemm_element(const uint8_t* qa, const float* sa, const uint8_t* qb,
         int64_t k1 = k0 + TILE < K ? k0 + TILE : K;
         double P = 0.0, Pabs = 0.0;
         for (int64_t k = k0; k < k1; ++k) {
-            double prod = fp8o_e4m3_decode(qa[m * K + k]) * fp8o_e4m3_decode(qb[n * K + k]);
+            double prod = dec[qa[m * K + k]] * dec[qb[n * K + k]];
             P += prod;
             Pabs += fabs(prod);
         }
@@ -234,6 +234,11 @@ static void gemm_element(const uint8_t* qa, const float* sa, const uint8_t* qb,
     *S = bound;
 }
 
+/* The 256 decoded code values, dec[c] = fp8o_e4m3_decode(c). */
+static void decode_table(double dec[256]) {
+    for (int c = 0; c < 256; ++c) dec[c] = fp8o_e4m3_decode((uint8_t)c);
+}
+
 /*
  * The GEMM at selected outputs: for i < nrows, j < ncols, the element
  * (rows[i], cols[j]) goes to c32[i * ncols + j] and its bound to S[...].
@@ -241,9 +246,11 @@ static void gemm_element(const uint8_t* qa, const float* sa, const uint8_t* qb,
 void fp8o_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb,
                int64_t K, const int64_t* rows, int64_t nrows, const int64_t* cols,
                int64_t ncols, float* c32, double* S) {
+    double dec[256];
+    decode_table(dec);
     for (int64_t i = 0; i < nrows; ++i)
         for (int64_t j = 0; j < ncols; ++j)
-            gemm_element(qa, sa, qb, sb, K, rows[i], cols[j], &c32[i * ncols + j],
+            gemm_element(dec, qa, sa, qb, sb, K, rows[i], cols[j], &c32[i * ncols + j],
                          &S[i * ncols + j]);
 }
 
@@ -262,6 +269,8 @@ void fp8o_grouped_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb,
                        int64_t ncols, float* c32, double* S) {
     int64_t KB = (K + TILE - 1) / TILE;
     int64_t NB = (N + TILE - 1) / TILE;
+    double dec[256];
+    decode_table(dec);
     for (int64_t i = 0; i < nrows; ++i) {
         int64_t m = rows[i];
         int32_t e = 0;
@@ -272,8 +281,8 @@ void fp8o_grouped_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb,
                 S[i * ncols + j] = NAN;
                 continue;
             }
-            gemm_element(qa, sa, qb + (int64_t)e * N * K, sb + (int64_t)e * NB * KB, K, m,
-                         cols[j], &c32[i * ncols + j], &S[i * ncols + j]);
+            gemm_element(dec, qa, sa, qb + (int64_t)e * N * K, sb + (int64_t)e * NB * KB, K,
+                         m, cols[j], &c32[i * ncols + j], &S[i * ncols + j]);
         }
     }
 }

@@ -1,0 +1,121 @@
+"""The C-ABI library builds for sm_103a, loads, exports every entry point
+declared in include/fp8q.h, and rejects bad arguments on the host before it
+touches CUDA. No kernel runs here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+from fp8_fine_grained_25_b300 import build as fbuild
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = fbuild.build()
+    return ctypes.CDLL(path)
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "fp8q.h")).read()
+    return re.findall(r"^FP8Q_API\s+[\w\s\*]*?\b(\w+)\s*\(", src, re.M)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert set(names) >= {"fp8q_quant_act", "fp8q_quant_weight", "fp8_block_gemm",
+                          "fp8_grouped_gemm", "fp8q_status_string"}
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_only_declared_symbols_are_exported():
+    out = os.popen(f"nm -D --defined-only {fbuild.LIB}").read()
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    assert exported == set(_declared())
+
+
+def test_status_strings(lib):
+    lib.fp8q_status_string.restype = ctypes.c_char_p
+    for code in range(9):
+        assert lib.fp8q_status_string(code)
+    assert b"unknown" in lib.fp8q_status_string(99)
+
+
+# Status codes, mirrored from include/fp8q.h.
+OK, NULL, SHAPE, ALIGN = 0, 1, 2, 3
+P = 1 << 20  # a 16-byte-aligned non-null fake pointer; never dereferenced on these paths
+
+
+def _q(lib, *a):
+    f = lib.fp8q_quant_act
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+                  ctypes.c_void_p, ctypes.c_void_p]
+    return f(*a)
+
+
+def _w(lib, *a):
+    f = lib.fp8q_quant_weight
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+                  ctypes.c_void_p, ctypes.c_void_p]
+    return f(*a)
+
+
+def _g(lib, *a):
+    f = lib.fp8_block_gemm
+    f.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int64] * 3 + [ctypes.c_void_p]
+    return f(*a)
+
+
+def _gg(lib, *a):
+    f = lib.fp8_grouped_gemm
+    f.argtypes = [ctypes.c_void_p] * 6 + [ctypes.c_int32] + [ctypes.c_int64] * 3 + [ctypes.c_void_p]
+    return f(*a)
+
+
+def test_quant_act_argument_checks(lib):
+    assert _q(lib, P, -1, 128, P, P, None) == SHAPE
+    assert _q(lib, P, 4, 0, P, P, None) == SHAPE
+    assert _q(lib, P, 4, 1 << 31, P, P, None) == SHAPE
+    assert _q(lib, None, 0, 128, None, None, None) == OK  # M = 0 is a no-op
+    assert _q(lib, None, 4, 128, P, P, None) == NULL
+    assert _q(lib, P, 4, 128, None, P, None) == NULL
+    assert _q(lib, P, 4, 128, P, None, None) == NULL
+    assert _q(lib, P, 4, 120, P, P, None) == ALIGN   # K % 16 != 0
+    assert _q(lib, P + 8, 4, 128, P, P, None) == ALIGN
+    assert _q(lib, P, 4, 128, P + 4, P, None) == ALIGN
+    assert _q(lib, P, 4, 128, P, P + 2, None) == ALIGN
+
+
+def test_quant_weight_argument_checks(lib):
+    assert _w(lib, P, -3, 128, P, P, None) == SHAPE
+    assert _w(lib, None, 0, 128, None, None, None) == OK
+    assert _w(lib, P, 4, 128, None, P, None) == NULL
+    assert _w(lib, P, 4, 24, P, P, None) == ALIGN
+
+
+def test_gemm_argument_checks(lib):
+    assert _g(lib, P, P, P, P, P, -1, 256, 512, None) == SHAPE
+    assert _g(lib, P, P, P, P, P, 128, 0, 512, None) == SHAPE
+    assert _g(lib, P, P, P, P, P, 128, 256, 0, None) == SHAPE
+    assert _g(lib, None, None, None, None, None, 0, 256, 512, None) == OK
+    for i in range(5):
+        args = [P] * 5
+        args[i] = None
+        assert _g(lib, *args, 128, 256, 512, None) == NULL
+    assert _g(lib, P, P, P, P, P, 128, 256, 520, None) == ALIGN   # K % 16
+    assert _g(lib, P, P, P, P, P, 128, 252, 512, None) == ALIGN   # N % 8
+    assert _g(lib, P + 8, P, P, P, P, 128, 256, 512, None) == ALIGN
+    assert _g(lib, P, P, P, P, P + 8, 128, 256, 512, None) == ALIGN
+
+
+def test_grouped_argument_checks(lib):
+    assert _gg(lib, P, P, P, P, P, P, 0, 64, 256, 512, None) == SHAPE      # E < 1
+    assert _gg(lib, P, P, P, P, P, P, 1025, 64, 256, 512, None) == SHAPE   # E > 1024
+    assert _gg(lib, P, P, P, P, P, P, 4, -1, 256, 512, None) == SHAPE
+    assert _gg(lib, P, P, P, P, P, P, 1024, 64, 1 << 22, 512, None) == SHAPE  # E*N > 2^31-1
+    assert _gg(lib, None, None, None, None, None, None, 4, 0, 256, 512, None) == OK
+    assert _gg(lib, P, P, P, P, P, None, 4, 64, 256, 512, None) == NULL
+    assert _gg(lib, P, P, P, P, P, P + 2, 4, 64, 256, 512, None) == ALIGN
+    assert _gg(lib, P, P, P, P, P, P, 4, 64, 256, 500, None) == ALIGN
