@@ -1,0 +1,404 @@
+"""Benchmark of the fine-grained FP8 hot path on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config C]
+
+One step is one pass of the whole path over one batch: quantize the bf16
+activations per 1x128 tile, quantize the bf16 weights per 128x128 block
+(weights change every training step, so they are re-quantized each step),
+and run the block-scaled FP8 GEMM with FP32 promotion. The default workload
+is the dense 7168-square layer (A [8192, 7168] with outlier channels,
+B [7168, 7168]); --config 4 times the grouped MoE GEMM path instead
+(32768 routed rows, 256 experts of [2048, 7168]).
+
+The printed JSON line reports whole-step TFLOP/s (2*M*N*K per step over the
+step time), the per-kernel times (CUDA events on the launching stream), the
+GEMM's roofline against the FP8 tensor peak, an end-to-end figure through
+the public API with pinned host buffers, the CPU oracle timed on a bounded
+sample of the same workload, and the SM clocks sampled during the timed
+region. Multi-GPU (torchrun): every rank runs its own copy of the workload
+(weak scaling, no collective on the data path); the time is the max over
+ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("block-scaled FP8 GEMM TFLOPS (% of B300 FP8 peak); quantize GB/s (% HBM)")
+FP8_OVER_BF16 = 2.0  # nominal dense FP8 : BF16 tensor throughput (4.5 : 2.25 PFLOP/s)
+FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            p = json.load(fh)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK), "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while running."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=5)
+
+    def summary(self):
+        mhz, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                mhz.append(float(parts[0]))
+                maxes.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[4:8]):
+                if flag.lower() == "active":
+                    reasons.add(name)
+        if not mhz:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": max(maxes),
+                "reasons": sorted(reasons), "samples": len(mhz)}
+
+
+# ---------------------------------------------------------------- workloads
+def make_workload(config: int, device):
+    from fp8_fine_grained_25_b300 import workloads
+    return workloads.CONFIGS[config](seed=0, device=device)
+
+
+def step_flops(w) -> float:
+    M, K = w.A.shape
+    if w.offsets is not None:
+        N = w.weights["W"].shape[1]
+    else:
+        N = next(iter(w.weights.values())).shape[0] if len(w.weights) == 1 else None
+    if N is None:  # several weights against the same A (MLA: Wq and Wkv)
+        return float(sum(2.0 * M * W.shape[0] * K for W in w.weights.values()))
+    return 2.0 * M * N * K
+
+
+class Path:
+    """The hot path on one device: buffers allocated once, one call per step."""
+
+    def __init__(self, w, device):
+        from fp8_fine_grained_25_b300 import fp8q
+        self.fp8q = fp8q
+        self.w = w
+        A = w.A
+        M, K = A.shape
+        self.qa = torch.empty((M, K), dtype=torch.uint8, device=device)
+        self.sa = torch.empty((M, -(-K // 128)), dtype=torch.float32, device=device)
+        self.bufs = {}
+        for name, W in w.weights.items():
+            qb = torch.empty(W.shape, dtype=torch.uint8, device=device)
+            if W.dim() == 3:
+                sb = torch.empty((W.shape[0], W.shape[1] // 128, -(-K // 128)), dtype=torch.float32,
+                                 device=device)
+                C = torch.empty((M, W.shape[1]), dtype=torch.bfloat16, device=device)
+            else:
+                sb = torch.empty((-(-W.shape[0] // 128), -(-K // 128)), dtype=torch.float32,
+                                 device=device)
+                C = torch.empty((M, W.shape[0]), dtype=torch.bfloat16, device=device)
+            self.bufs[name] = (qb, sb, C)
+        self.launches_per_step = 1 + 2 * len(w.weights)
+
+    def step(self, A=None, weights=None, events=None):
+        f = self.fp8q
+        A = self.w.A if A is None else A
+        weights = self.w.weights if weights is None else weights
+        rec = (lambda i: events[i].record()) if events is not None else (lambda i: None)
+        rec(0)
+        f.fp8q_quant_act(A, self.qa, self.sa)
+        rec(1)
+        i = 2
+        for name, W in weights.items():
+            qb, sb, _ = self.bufs[name]
+            f.fp8q_quant_weight(W, qb, sb)
+            rec(i)
+            i += 1
+        for name in weights:
+            qb, sb, C = self.bufs[name]
+            if self.w.offsets is not None:
+                f.fp8_grouped_gemm(self.qa, self.sa, qb, sb, self.w.offsets, C)
+            else:
+                f.fp8_block_gemm(self.qa, self.sa, qb, sb, C)
+            rec(i)
+            i += 1
+
+
+# --------------------------------------------------------------- CPU oracle
+def oracle_sample(w, rows_a: int, rows_b: int, out_rows: int, threads: int):
+    """Time the CPU oracle on a bounded sample of one step and extrapolate
+    the full step: quantizer time scales with elements, GEMM time with
+    output elements. Returns (seconds for a full step, description)."""
+    import numpy as np
+    import oracle
+    A = w.A
+    M, K = A.shape
+    Wd = w.weights["W"][0] if w.offsets is not None else next(iter(w.weights.values()))
+    N = Wd.shape[0]
+    bits = lambda t: t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    a_s = bits(A[:rows_a])
+    b_s = bits(Wd[:rows_b])
+    t0 = time.perf_counter()
+    qa, sa = oracle.quant_act(a_s, threads=threads)
+    t1 = time.perf_counter()
+    qb_full, sb_full = oracle.quant_weight(bits(Wd), threads=threads)  # GEMM needs all of B
+    t2 = time.perf_counter()
+    c32, S = oracle.gemm(qa, sa, qb_full, sb_full, rows=np.arange(min(out_rows, rows_a)),
+                         threads=threads)
+    t3 = time.perf_counter()
+    w_elems = sum(W.numel() for W in w.weights.values())
+    full = ((t1 - t0) * (M * K) / a_s.size
+            + (t2 - t1) * w_elems / Wd.numel()
+            + (t3 - t2) * (step_flops(w) / (2.0 * min(out_rows, rows_a) * N * K)))
+    desc = (f"oracle quant_act on {rows_a}x{K} rows, quant_weight on one [{N}x{K}] weight, "
+            f"GEMM on {min(out_rows, rows_a)} output rows x {N} columns; "
+            f"sample took {t3 - t0:.2f} s, full step extrapolated by element counts")
+    return full, desc
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the CPU oracle, as it stands, on this machine's cores."""
+    if rank != 0:
+        return
+    threads = os.cpu_count() or 1
+    w = make_workload(args.config, "cpu")
+    flops = step_flops(w)
+    times = []
+    desc = ""
+    for i in range(args.warmup + args.steps):
+        full, desc = oracle_sample(w, rows_a=64, rows_b=128, out_rows=4, threads=threads)
+        if i >= args.warmup:
+            times.append(full)
+    t = statistics.median(times)
+    value = flops / t / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64/f32", "data": "synthetic",
+            "config": {"workload": w.name},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    peaks, peak_kind = load_peaks()
+
+    w = make_workload(args.config, device)
+    path = Path(w, device)
+    flops = step_flops(w)
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        path.step()
+    torch.cuda.synchronize()
+    assert path.fp8q.fp8q_get_device_status() == 0
+
+    nev = 1 + path.launches_per_step
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(device.index) as clocks:
+        start.record(stream)
+        for i in range(args.steps):
+            path.step(events=events[i])
+        stop.record(stream)
+        torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    elapsed = start.elapsed_time(stop) / 1e3
+    if dist is not None:
+        t = torch.tensor([elapsed], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed = float(t.item())
+    status = path.fp8q.fp8q_get_device_status()
+
+    # per-kernel averages from the events around each launch
+    names = ["quant_act"] + [f"quant_weight[{n}]" for n in w.weights] + \
+            [f"gemm[{n}]" for n in w.weights]
+    per = {n: statistics.fmean(ev[j].elapsed_time(ev[j + 1]) for ev in events) / 1e3
+           for j, n in enumerate(names)}
+
+    M, K = w.A.shape
+    kern = {}
+    kern["quant_act"] = {"ms": per["quant_act"] * 1e3,
+                         "GB/s": (3 * M * K + 4 * M * -(-K // 128)) / per["quant_act"] / 1e9}
+    for n, W in w.weights.items():
+        e = W.numel()
+        blocks = e // W.shape[-1] // 128 * -(-W.shape[-1] // 128)
+        tq = per[f"quant_weight[{n}]"]
+        kern[f"quant_weight[{n}]"] = {"ms": tq * 1e3, "GB/s": (3 * e + 4 * blocks) / tq / 1e9}
+        N = W.shape[-2]
+        tg = per[f"gemm[{n}]"]
+        kern[f"gemm[{n}]"] = {"ms": tg * 1e3, "TFLOP/s": 2.0 * M * N * K / tg / 1e12}
+    for v in kern.values():
+        if "GB/s" in v:
+            v["frac_hbm"] = v["GB/s"] / peaks["hbm_gbs"]
+
+    # dominant kernel: the GEMM(s)
+    gemm_names = [f"gemm[{n}]" for n in w.weights]
+    t_gemm = sum(per[n] for n in gemm_names)
+    fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+    gemm_tflops = flops / t_gemm / 1e12
+    roofline = {"bound": "tensor", "achieved": gemm_tflops, "peak": fp8_peak, "unit": "TFLOP/s",
+                "frac": gemm_tflops / fp8_peak, "traffic": None,
+                "kernel": "fp8_gemm_kernel", "peak_source":
+                    f"{peak_kind} bf16 burst {peaks['bf16_tflops']} TFLOP/s x {FP8_OVER_BF16} "
+                    "(nominal FP8:BF16 ratio)"}
+    if w.offsets is not None:
+        # the grouped GEMM streams every expert's weights once: HBM-bound
+        wbytes = w.weights["W"].numel() + 4 * w.weights["W"].numel() // 16384
+        abytes = M * K + 2 * M * w.weights["W"].shape[1]
+        roofline["hbm_GB/s"] = (wbytes + abytes) / t_gemm / 1e9
+        roofline["hbm_frac"] = roofline["hbm_GB/s"] / peaks["hbm_gbs"]
+
+    ms_per_step = elapsed / args.steps * 1e3
+    value = world * flops * args.steps / elapsed / 1e12
+
+    # end to end through the public API: pinned host inputs in, C back out
+    e2e = None
+    if args.e2e_steps > 0:
+        hostA = w.A.cpu().pin_memory()
+        hostW = {n: W.cpu().pin_memory() for n, W in w.weights.items()}
+        devA = torch.empty_like(w.A)
+        devW = {n: torch.empty_like(W) for n, W in w.weights.items()}
+        hostC = {n: torch.empty(path.bufs[n][2].shape, dtype=torch.bfloat16).pin_memory()
+                 for n in w.weights}
+        def e2e_step():
+            devA.copy_(hostA, non_blocking=True)
+            for n in w.weights:
+                devW[n].copy_(hostW[n], non_blocking=True)
+            path.step(A=devA, weights=devW)
+            for n in w.weights:
+                hostC[n].copy_(path.bufs[n][2], non_blocking=True)
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        te = s0.elapsed_time(s1) / 1e3
+        if dist is not None:
+            t = torch.tensor([te], device=device)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            te = float(t.item())
+        e2e = {"value": world * flops * args.e2e_steps / te / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": hostA.numel() * 2 + sum(v.numel() * 2 for v in hostW.values()),
+               "d2h_bytes_per_step": sum(v.numel() * 2 for v in hostC.values()),
+               "ms_per_step": te / args.e2e_steps * 1e3}
+
+    cpu = None
+    if rank == 0 and world == 1:
+        threads = os.cpu_count() or 1
+        full, desc = oracle_sample(w, rows_a=256, rows_b=128, out_rows=128, threads=threads)
+        cpu = {"value": flops / full / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": desc}
+
+    if rank == 0:
+        a_bytes = w.A.numel() * 2 + sum(W.numel() * 2 for W in w.weights.values())
+        line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "e4m3*e4m3->f32", "data": "synthetic",
+                "config": {"workload": w.name + ": quant_act(A) + quant_weight(W) + "
+                           + ("grouped" if w.offsets is not None else "dense")
+                           + " block-scaled GEMM per step",
+                           "parallelism": f"replicas x{world}",
+                           "l2": f"inputs larger than L2 (bf16 inputs {a_bytes / 1e6:.0f} MB "
+                                 "re-read every step)"},
+                "roofline": roofline, "kernels": kern, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": path.launches_per_step * args.steps,
+                "clocks": clocks.summary(), "device_status": status,
+                "peaks": {"source": peak_kind, "hbm_gbs": peaks["hbm_gbs"],
+                          "fp8_tflops": fp8_peak}}
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
