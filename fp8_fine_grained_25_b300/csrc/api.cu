@@ -67,10 +67,10 @@ EncodeTiledFn encode_tiled() {
 }
 
 // A row-major [outer, inner] tensor, boxes of [box_outer, box_inner]
-// elements, 128-byte swizzle, zero fill outside the tensor.
+// elements, swizzled shared-memory layout, zero fill outside the tensor.
 bool make_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, uint64_t elem_bytes,
                  const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
-                 uint32_t box_outer) {
+                 uint32_t box_outer, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
     EncodeTiledFn fn = encode_tiled();
     if (!fn) return false;
     const cuuint64_t dims[2] = {inner, outer};
@@ -78,7 +78,7 @@ bool make_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, uint64_t elem_byte
     const cuuint32_t box[2] = {box_inner, box_outer};
     const cuuint32_t elem_strides[2] = {1, 1};
     return fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, elem_strides,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -181,7 +181,8 @@ int fp8_block_gemm(const void* A, const float* sa, const void* B, const float* s
     CUtensorMap tmA, tmB, tmC;
     if (!make_map_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, K, M, 128, 128) ||
         !make_map_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, K, N, 128, bn) ||
-        !make_map_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C_bf16, N, M, 64, 32))
+        !make_map_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C_bf16, N, M, 32, 32,
+                     CU_TENSOR_MAP_SWIZZLE_64B))
         return FP8Q_ERR_CUDA;
 
     fp8q::GemmLaunch g{};

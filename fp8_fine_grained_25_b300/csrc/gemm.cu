@@ -4,23 +4,27 @@
 // "FP8 低精度训练": "细粒度量化" Fig. 7a for the scale granularity,
 // "提高累加精度" Fig. 7b for the promotion into FP32 registers).
 //
-// Per CTA (persistent, one 128 x BN output tile at a time):
+// Per CTA (persistent, one 128 x BN output tile at a time, 12 warps):
 //   warp 0      TMA producer: per K block, a 128x128 A box and a BNx128 B box
 //               (E4M3, 128-byte swizzle) into a ring of shared-memory stages.
-//   warp 1      MMA issuer (one thread): 4 x tcgen05.mma kind::f8f6f4
-//               (K = 32 each) write P_kb = A_kb * B_kb^T into one of two TMEM
-//               buffers (fresh accumulate per K block), then commit to the
-//               stage's "empty" barrier and the buffer's "full" barrier.
-//               The same warp allocates and frees TMEM.
+//   warp 1      MMA issuer: 4 x tcgen05.mma kind::f8f6f4 (K = 32 each) write
+//               P_kb = A_kb * B_kb^T into one of 512/BN TMEM buffers (fresh
+//               accumulate per K block), then commit to the stage's "empty"
+//               barrier and the buffer's "full" barrier. Allocates and frees
+//               TMEM. The warp stays converged and one elected lane issues.
+//   warp 2      scale loader: per K block, cp.async copies of sa[m0..m0+127][kb]
+//               and the tile's sb[nb][kb] into a shared-memory scale ring, so
+//               the promotion never waits on a global load.
 //   warps 4-11  promotion + epilogue: tcgen05.ld P_kb (each warp owns 32
 //               TMEM lanes = 32 rows and half of the BN columns), then
-//               acc += P_kb * (sa[m][kb] * sb[n/128][kb]) in FP32 registers,
-//               release the TMEM buffer, and after the last K block convert
-//               to bf16 and store (TMA store for the dense GEMM, masked
-//               vector stores for the grouped one).
-// Double-buffered TMEM lets the MMA of K block kb+1 overlap the promotion of
-// block kb. Every wait is bounded in time; on expiry the CTA raises an
-// abort flag, drains its copies and MMAs, frees TMEM and returns.
+//               acc += P_kb * (sa[m][kb] * sb[n/128][kb]) with packed FP32
+//               FMAs into registers, release the TMEM buffer; after the last
+//               K block convert to bf16 and store (TMA store through a small
+//               swizzled staging buffer for the dense GEMM, masked vector
+//               stores for the grouped one).
+// Several TMEM buffers let the MMA of later K blocks overlap the promotion
+// of earlier ones. Every wait is bounded in time; on expiry the CTA raises
+// an abort flag, drains its copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -39,35 +43,46 @@ namespace {
 constexpr int BM = 128;
 constexpr int BK = 128;
 constexpr int kThreads = 384;
+constexpr int kScaleWarp = 2;
 constexpr int kFirstEpiWarp = 4;
 constexpr int kEpiWarps = 8;
-constexpr int kGroupM = 16;  // rasterisation: m-tiles per group for L2 reuse
+constexpr int kGroupM = 16;     // rasterisation: m-tiles per group for L2 reuse
 constexpr int kSmemLimit = 232448;
 constexpr int kCtrlRegs = 40, kEpiRegs = 232;  // setmaxnreg split: 128*40 + 256*232 = 384*168
+constexpr int kScaleSlots = 8;  // K blocks of scales staged ahead
+constexpr int kMaxNb = 4;       // 128-column blocks one tile can touch (BN <= 256: at most 3)
 
 template <int BN, bool GROUPED>
 struct Layout {
     static constexpr int A_BYTES = BM * BK;
     static constexpr int B_BYTES = BN * BK;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int EPI_WARP_BYTES = 32 * 64 * 2;  // 32 rows x 64 bf16 columns
+    static constexpr int EPI_WARP_BYTES = 32 * 32 * 2;  // 32 rows x 32 bf16, 64-byte swizzle
     static constexpr int EPI_BYTES = GROUPED ? 0 : kEpiWarps * EPI_WARP_BYTES;
-    static constexpr int RESERVE = 1024 /*alignment slack*/ + 256 /*barriers, flags*/ +
+    static constexpr int SCALE_SLOT_BYTES = 4 * (BM + kMaxNb);  // sa[128] then sb[kMaxNb]
+    static constexpr int SCALE_BYTES = kScaleSlots * SCALE_SLOT_BYTES;
+    static constexpr int NBUF = (512 / BN) > 4 ? 4 : (512 / BN);  // TMEM buffers of BN columns
+    static constexpr int TMEM_COLS = NBUF * BN <= 128 ? 128 : NBUF * BN <= 256 ? 256 : 512;
+    static constexpr int RESERVE = 1024 /*alignment slack*/ + 512 /*barriers, flags*/ +
                                    (GROUPED ? 4 * (kMaxExperts + 1) : 0);
-    static constexpr int STAGES_FIT = (kSmemLimit - RESERVE - EPI_BYTES) / STAGE_BYTES;
+    static constexpr int STAGES_FIT =
+        (kSmemLimit - RESERVE - EPI_BYTES - SCALE_BYTES) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
     static constexpr int EPI_OFF = STAGES * STAGE_BYTES;
-    static constexpr int BAR_OFF = EPI_OFF + EPI_BYTES;
-    // barriers: full[S], empty[S], tmem_full[2], tmem_empty[2], drain
-    static constexpr int NUM_BARS = 2 * STAGES + 5;
+    static constexpr int SCALE_OFF = EPI_OFF + EPI_BYTES;
+    static constexpr int BAR_OFF = SCALE_OFF + SCALE_BYTES;
+    // barriers: full[S], empty[S], tmem_full[NBUF], tmem_empty[NBUF],
+    // scale_full[slots], scale_empty[slots], drain
+    static constexpr int FULL = 0, EMPTY = STAGES, TFULL = 2 * STAGES, TEMPTY = TFULL + NBUF,
+                         SFULL = TEMPTY + NBUF, SEMPTY = SFULL + kScaleSlots,
+                         DRAIN = SEMPTY + kScaleSlots, NUM_BARS = DRAIN + 1;
     static constexpr int MISC_OFF = BAR_OFF + 8 * NUM_BARS;  // tmem slot, abort flag
     static constexpr int TABLE_OFF = MISC_OFF + 16;
-    static constexpr int TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
-                                     : (2 * BN <= 256) ? 256 : 512;
-    static constexpr int HALF = BN / 2;  // columns per promotion warp
-    static constexpr int CHUNKS = HALF / 32;
-    static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN must be 64..256 in steps of 64");
+    static constexpr int HALF = BN / 2;       // columns per promotion warp
+    static constexpr int CHUNKS = HALF / 32;  // 32-column TMEM loads, issued in pairs
+    static_assert(BN == 128 || BN == 256, "tile width must be 128 or 256");
     static_assert(STAGES >= 2, "not enough shared memory for two stages");
+    static_assert(8 * NUM_BARS + 16 <= 512, "barrier area overflow");
     static constexpr int smem_bytes(int E) {
         return TABLE_OFF + (GROUPED ? 4 * (E + 1) : 0) + 1024;
     }
@@ -155,12 +170,20 @@ __device__ void build_group_table(const GemmArgs& a, int* table) {
     }
 }
 
+// A bounded wait taken by a whole warp: true only if every lane saw the
+// phase complete (the lanes may disagree only at the time limit).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          uint64_t limit) {
+    return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, abort_flag, limit));
+}
+
 template <int BN, bool GROUPED>
 __global__ void __launch_bounds__(kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
     using L = Layout<BN, GROUPED>;
     constexpr int S = L::STAGES;
+    constexpr int NBUF = L::NBUF;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
@@ -168,7 +191,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sbase = raw + pad;
 
     auto bar = [&](int i) -> uint32_t { return sbase + L::BAR_OFF + 8u * i; };
-    const int FULL = 0, EMPTY = S, TFULL = 2 * S, TEMPTY = 2 * S + 2, DRAIN = 2 * S + 4;
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + L::MISC_OFF);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::MISC_OFF + 4);
     int* table = reinterpret_cast<int*>(smem + L::TABLE_OFF);
@@ -179,14 +201,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(bar(FULL + s), 1);
-            mbar_init(bar(EMPTY + s), 1);
+            mbar_init(bar(L::FULL + s), 1);
+            mbar_init(bar(L::EMPTY + s), 1);
         }
-        mbar_init(bar(TFULL + 0), 1);
-        mbar_init(bar(TFULL + 1), 1);
-        mbar_init(bar(TEMPTY + 0), kEpiWarps);
-        mbar_init(bar(TEMPTY + 1), kEpiWarps);
-        mbar_init(bar(DRAIN), 1);
+        for (int b = 0; b < NBUF; ++b) {
+            mbar_init(bar(L::TFULL + b), 1);
+            mbar_init(bar(L::TEMPTY + b), kEpiWarps);
+        }
+        for (int j = 0; j < kScaleSlots; ++j) {
+            mbar_init(bar(L::SFULL + j), 32);  // one cp.async completion arrive per lane
+            mbar_init(bar(L::SEMPTY + j), kEpiWarps);
+        }
+        mbar_init(bar(L::DRAIN), 1);
         *abort_flag = 0;
         fence_barrier_init();
         fence_proxy_async_smem();
@@ -201,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_relinquish_alloc_permit();
     }
     if constexpr (GROUPED) {
-        if (warp == 2) build_group_table(args, table);
+        if (warp == 3) build_group_table(args, table);
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -211,32 +237,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int KB = args.KB;
 
     // Registers: 384 threads launch with 168 each (64512). The control
-    // warpgroup (producer, MMA, two idle warps) gives most of its share to
-    // the two promotion warpgroups, which hold a 128 x BN/2 FP32 accumulator
-    // slice (BN/2 registers per thread) plus a 32-column TMEM chunk:
-    // 128 * 40 + 256 * 232 = 64512.
-    if (warp < kFirstEpiWarp) setmaxnreg_dec<kCtrlRegs>();
-
-    if (warp == 0) {
-        // ------------------------------------------------------ TMA producer
-        if (lane == 0) {
+    // warpgroup (producer, MMA, scale loader, one idle warp) gives most of its
+    // share to the two promotion warpgroups, which hold a 128 x BN/2 FP32
+    // accumulator slice (BN/2 registers per thread) plus two 32-column TMEM
+    // chunks: 128 * 40 + 256 * 232 = 64512.
+    if (warp < kFirstEpiWarp) {
+        setmaxnreg_dec<kCtrlRegs>();
+        if (warp == 0) {
+            // -------------------------------------------------- TMA producer
             int stage = 0;
-            uint32_t phase = 0;
-            uint32_t issued = 0;
+            uint32_t phase = 0, issued = 0;
             bool ok = true;
             for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
                 const Tile tile = decode_tile<BN, GROUPED>(args, table, t);
                 for (int kb = 0; kb < KB; ++kb) {
-                    if (!mbar_wait(bar(EMPTY + stage), phase ^ 1u, abort_flag, limit)) {
+                    if (!warp_wait(bar(L::EMPTY + stage), phase ^ 1u, abort_flag, limit)) {
                         ok = false;
                         break;
                     }
-                    uint32_t bytes = L::STAGE_BYTES;
-                    if ((args.debug & 1u) && issued == 0) bytes += 16;  // never-completing phase
-                    mbar_arrive_expect_tx(bar(FULL + stage), bytes);
-                    const uint32_t sA = sbase + stage * L::STAGE_BYTES;
-                    tma_load_2d(sA, &tmA, bar(FULL + stage), kb * BK, tile.m0);
-                    tma_load_2d(sA + L::A_BYTES, &tmB, bar(FULL + stage), kb * BK, tile.brow);
+                    if (elect_one()) {
+                        uint32_t bytes = L::STAGE_BYTES;
+                        if ((args.debug & 1u) && issued == 0) bytes += 16;  // never-completing phase
+                        mbar_arrive_expect_tx(bar(L::FULL + stage), bytes);
+                        const uint32_t sA = sbase + stage * L::STAGE_BYTES;
+                        tma_load_2d(sA, &tmA, bar(L::FULL + stage), kb * BK, tile.m0);
+                        tma_load_2d(sA + L::A_BYTES, &tmB, bar(L::FULL + stage), kb * BK, tile.brow);
+                    }
+                    __syncwarp();
                     ++issued;
                     if (++stage == S) {
                         stage = 0;
@@ -250,20 +277,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (static_cast<uint32_t>(s) >= issued) break;
                 const uint32_t last = s + S * ((issued - 1 - s) / S);
                 volatile int local_flag = 0;
-                mbar_wait(bar(FULL + s), (last / S) & 1u, &local_flag, limit);
+                mbar_wait(bar(L::FULL + s), (last / S) & 1u, &local_flag, limit);
             }
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------------- MMA issuer
-        if (lane == 0) {
+        } else if (warp == 1) {
+            // --------------------------------------------------- MMA issuer
             constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
             int stage = 0;
             uint32_t phase = 0, abuf = 0, aphase = 0;
             bool ok = true, issued_any = false;
             for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
                 for (int kb = 0; kb < KB; ++kb) {
-                    if (!mbar_wait(bar(TEMPTY + abuf), aphase ^ 1u, abort_flag, limit) ||
-                        !mbar_wait(bar(FULL + stage), phase, abort_flag, limit)) {
+                    if (!warp_wait(bar(L::TEMPTY + abuf), aphase ^ 1u, abort_flag, limit) ||
+                        !warp_wait(bar(L::FULL + stage), phase, abort_flag, limit)) {
                         ok = false;
                         break;
                     }
@@ -272,106 +297,168 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t ad = sdesc_k_sw128(sA);
                     const uint64_t bd = sdesc_k_sw128(sA + L::A_BYTES);
                     const uint32_t d = tmem_base + abuf * BN;
+                    if (elect_one()) {
 #pragma unroll
-                    for (int k = 0; k < BK / 32; ++k)
-                        mma_e4m3(d, ad + 2u * k, bd + 2u * k, idesc, k > 0 ? 1u : 0u);
-                    mma_commit(bar(EMPTY + stage));
-                    mma_commit(bar(TFULL + abuf));
+                        for (int k = 0; k < BK / 32; ++k)
+                            mma_e4m3(d, ad + 2u * k, bd + 2u * k, idesc, k > 0 ? 1u : 0u);
+                        mma_commit(bar(L::EMPTY + stage));
+                        mma_commit(bar(L::TFULL + abuf));
+                    }
+                    __syncwarp();
                     issued_any = true;
                     if (++stage == S) {
                         stage = 0;
                         phase ^= 1u;
                     }
-                    abuf ^= 1u;
-                    if (abuf == 0) aphase ^= 1u;
+                    if (++abuf == NBUF) {
+                        abuf = 0;
+                        aphase ^= 1u;
+                    }
                 }
             }
             // Every MMA issued above has completed once this arrives.
             if (issued_any) {
-                mma_commit(bar(DRAIN));
+                if (elect_one()) mma_commit(bar(L::DRAIN));
+                __syncwarp();
                 volatile int local_flag = 0;
-                mbar_wait(bar(DRAIN), 0, &local_flag, limit);
+                mbar_wait(bar(L::DRAIN), 0, &local_flag, limit);
             }
+        } else if (warp == kScaleWarp) {
+            // ------------------------------------------------- scale loader
+            // Slot j holds, for one K block, sa of the tile's 128 rows (row r
+            // at float r) and sb of the tile's 128-column blocks from n0/128
+            // on (at floats 128..131). Rows outside the tile and blocks past
+            // the last one are written as zero.
+            int slot = 0;
+            uint32_t sphase = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+                const Tile tile = decode_tile<BN, GROUPED>(args, table, t);
+                const float* sb_e = args.sb + static_cast<int64_t>(tile.e) * args.NB * KB;
+                const int nb = (tile.n0 >> 7) + lane;
+                const bool sb_ok = lane < kMaxNb && nb < args.NB && (nb << 7) < tile.n0 + BN;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!warp_wait(bar(L::SEMPTY + slot), sphase ^ 1u, abort_flag, limit)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sl = sbase + L::SCALE_OFF + slot * L::SCALE_SLOT_BYTES;
+#pragma unroll
+                    for (int i = 0; i < BM / 32; ++i) {
+                        const int r = lane + 32 * i;
+                        const int m = tile.m0 + r;
+                        const bool live = m < tile.row_end;
+                        const float* src = args.sa + (live ? static_cast<int64_t>(m) * KB + kb : 0);
+                        cp_async_4(sl + 4u * r, src, live ? 4u : 0u);
+                    }
+                    if (lane < kMaxNb) {
+                        const float* src = sb_e + (sb_ok ? static_cast<int64_t>(nb) * KB + kb : 0);
+                        cp_async_4(sl + 4u * (BM + lane), src, sb_ok ? 4u : 0u);
+                    }
+                    cp_async_mbar_arrive(bar(L::SFULL + slot));
+                    if (++slot == kScaleSlots) {
+                        slot = 0;
+                        sphase ^= 1u;
+                    }
+                }
+            }
+            // Let the last copies land before the CTA may exit.
+            asm volatile("cp.async.wait_all;" ::: "memory");
         }
-    } else if (warp >= kFirstEpiWarp) {
-        // ------------------------------------------- promotion + epilogue
+    } else {
+        // --------------------------------------------- promotion + epilogue
         setmaxnreg_inc<kEpiRegs>();
         const int ew = warp - kFirstEpiWarp;  // 0..7
         const int quarter = warp & 3;         // TMEM lanes 32*quarter .. +31
         const int h = ew >> 2;                // column half
         const int row = quarter * 32 + lane;  // row inside the tile
         const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+        const float* scale_ring = reinterpret_cast<const float*>(smem + L::SCALE_OFF);
         uint32_t abuf = 0, aphase = 0;
+        int slot = 0;
+        uint32_t sphase = 0;
         bool ok = true;
         for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
             const Tile tile = decode_tile<BN, GROUPED>(args, table, t);
             const int m = tile.m0 + row;
             const bool row_ok = m < tile.row_end;
-            const float* sa_row = args.sa + static_cast<int64_t>(row_ok ? m : 0) * KB;
-            const float* sb_e = args.sb + static_cast<int64_t>(tile.e) * args.NB * KB;
             const int col0 = tile.n0 + h * L::HALF;  // first column of this warp
-            int nbk[L::CHUNKS];
-#pragma unroll
-            for (int c = 0; c < L::CHUNKS; ++c) {
-                const int nb = (col0 + 32 * c) >> 7;
-                nbk[c] = nb < args.NB ? nb * KB : -1;
-            }
             float acc[L::HALF];
 #pragma unroll
             for (int j = 0; j < L::HALF; ++j) acc[j] = 0.0f;
 
             for (int kb = 0; kb < KB; ++kb) {
-                const float a_s = row_ok ? __ldg(sa_row + kb) : 0.0f;
+                // scales of this K block, from the ring (staged ahead)
+                if (!warp_wait(bar(L::SFULL + slot), sphase, abort_flag, limit)) {
+                    ok = false;
+                    break;
+                }
+                const float* sl = scale_ring + slot * (L::SCALE_SLOT_BYTES / 4);
+                const float a_s = sl[row];
                 float cs[L::CHUNKS];
 #pragma unroll
                 for (int c = 0; c < L::CHUNKS; ++c)
-                    cs[c] = nbk[c] >= 0 ? a_s * __ldg(sb_e + nbk[c] + kb) : 0.0f;
-                const bool got = mbar_wait(bar(TFULL + abuf), aphase, abort_flag, limit);
-                if (!__all_sync(0xFFFFFFFFu, got)) {
+                    cs[c] = a_s * sl[BM + ((h * L::HALF + 32 * c) >> 7)];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(L::SEMPTY + slot));
+                if (++slot == kScaleSlots) {
+                    slot = 0;
+                    sphase ^= 1u;
+                }
+
+                if (!warp_wait(bar(L::TFULL + abuf), aphase, abort_flag, limit)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
                 const uint32_t taddr = lane_base + abuf * BN + h * L::HALF;
 #pragma unroll
-                for (int c = 0; c < L::CHUNKS; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(taddr + 32 * c, r);
-                    tmem_wait_ld32(r);
+                for (int c = 0; c < L::CHUNKS; c += 2) {
+                    uint32_t r0[32], r1[32];
+                    tmem_ld32(taddr + 32 * c, r0);
+                    tmem_ld32(taddr + 32 * (c + 1), r1);
+                    tmem_wait_ld64(r0, r1);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        acc[32 * c + j] = fmaf(__uint_as_float(r[j]), cs[c], acc[32 * c + j]);
+                    for (int j = 0; j < 32; j += 2)
+                        ffma2(acc[32 * c + j], acc[32 * c + j + 1], r0[j], r0[j + 1], cs[c]);
+#pragma unroll
+                    for (int j = 0; j < 32; j += 2)
+                        ffma2(acc[32 * (c + 1) + j], acc[32 * (c + 1) + j + 1], r1[j], r1[j + 1],
+                              cs[c + 1]);
                 }
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(TEMPTY + abuf));
-                abuf ^= 1u;
-                if (abuf == 0) aphase ^= 1u;
+                if (lane == 0) mbar_arrive(bar(L::TEMPTY + abuf));
+                if (++abuf == NBUF) {
+                    abuf = 0;
+                    aphase ^= 1u;
+                }
             }
             if (!ok) break;
 
             if constexpr (!GROUPED) {
-                // bf16 -> swizzled staging (32 rows x 128 B per warp) -> TMA store
+                // bf16 -> 64-byte-swizzled staging (32 rows x 64 B per warp)
+                // -> TMA store, 32 columns at a time
                 uint8_t* ebuf = smem + L::EPI_OFF + ew * L::EPI_WARP_BYTES;
                 const uint32_t ebuf_s = sbase + L::EPI_OFF + ew * L::EPI_WARP_BYTES;
 #pragma unroll
-                for (int c2 = 0; c2 < L::HALF / 64; ++c2) {
+                for (int c2 = 0; c2 < L::HALF / 32; ++c2) {
                     if (lane == 0) bulk_wait_group_read0();
                     __syncwarp();
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const float* v = acc + 64 * c2 + 8 * j;
+                    for (int j = 0; j < 4; ++j) {
+                        const float* v = acc + 32 * c2 + 8 * j;
                         uint4 pk;
                         pk.x = pack_bf16x2(v[0], v[1]);
                         pk.y = pack_bf16x2(v[2], v[3]);
                         pk.z = pack_bf16x2(v[4], v[5]);
                         pk.w = pack_bf16x2(v[6], v[7]);
-                        const int phys = j ^ (lane & 7);
-                        *reinterpret_cast<uint4*>(ebuf + lane * 128 + phys * 16) = pk;
+                        const int phys = j ^ ((lane >> 1) & 3);
+                        *reinterpret_cast<uint4*>(ebuf + lane * 64 + phys * 16) = pk;
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
-                    const int x = col0 + 64 * c2, y = tile.m0 + quarter * 32;
+                    const int x = col0 + 32 * c2, y = tile.m0 + quarter * 32;
                     if (lane == 0 && x < args.N && y < args.M) {
                         tma_store_2d(&tmC, ebuf_s, x, y);
                         bulk_commit_group();

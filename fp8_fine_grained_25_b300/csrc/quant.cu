@@ -11,6 +11,8 @@
 //   amax  = max |x|                 (bf16 -> fp32 is exact, max is exact)
 //   s     = fl32(amax / 448)        (IEEE round-to-nearest divide)
 //   q_i   = E4M3_rn_satfinite(fl32(x_i / s)),  all-zero tile: s = 0, q = 0
+// The per-element quotient uses the tile's reciprocal and one FMA
+// correction instead of a full divide (see div_by_scale).
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
@@ -45,12 +47,36 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
         __nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3));
 }
 
+// x / s rounded to nearest, from r = RN(1/s) and one exact-residual
+// correction (Markstein, "Computation of elementary functions on the IBM
+// RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990):
+//   q0 = RN(x * r);  e = RN(q0 * s - x) (exact);  q = RN(q0 - e * r).
+// Writing the residual negated keeps the sign of a zero quotient (-0 / s
+// gives -0). For every bf16 x with |x| <= amax and every bf16 amax >= 2^-90
+// this equals the IEEE quotient whenever |x / s| >= 2^-12; smaller
+// quotients may differ in the last bits but keep their sign, and all of
+// them encode to a signed E4M3 zero either way.
+__device__ __forceinline__ float div_by_scale(float x, float s, float r) {
+    const float q0 = __fmul_rn(x, r);
+    const float e = __fmaf_rn(q0, s, -x);
+    return __fmaf_rn(-e, r, q0);
+}
+
+constexpr float kFastDivMinAmax = 0x1p-90f;
+
 // Eight values divided by the tile scale and encoded, low byte first.
-__device__ __forceinline__ uint2 encode8(const float (&f)[8], float s) {
+// `amax` is the tile's absolute maximum (s = amax / 448).
+__device__ __forceinline__ uint2 encode8(const float (&f)[8], float s, float amax) {
     if (s == 0.0f) return make_uint2(0u, 0u);
     float y[8];
+    if (amax >= kFastDivMinAmax) {
+        const float r = __frcp_rn(s);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) y[i] = __fdiv_rn(f[i], s);
+        for (int i = 0; i < 8; ++i) y[i] = div_by_scale(f[i], s, r);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) y[i] = __fdiv_rn(f[i], s);
+    }
     uint2 out;
     out.x = e4m3x2(y[0], y[1]) | (e4m3x2(y[2], y[3]) << 16);
     out.y = e4m3x2(y[4], y[5]) | (e4m3x2(y[6], y[7]) << 16);
@@ -105,7 +131,7 @@ __global__ void __launch_bounds__(kActThreads) quant_act_kernel(const uint8_t* _
             const float sc = __fdiv_rn(amax, 448.0f);
             const uint64_t t = base + 2 * u + half;
             if (live[u]) {
-                *reinterpret_cast<uint2*>(q + off[u]) = encode8(f, sc);
+                *reinterpret_cast<uint2*>(q + off[u]) = encode8(f, sc, amax);
                 if (sub == 0) s[t] = sc;
             }
         }
@@ -161,7 +187,7 @@ __global__ void __launch_bounds__(kWThreads) quant_weight_kernel(const uint8_t* 
             if (!live[i]) continue;
             float f[8];
             unpack_bf16x8(v[i], f);
-            *reinterpret_cast<uint2*>(q + off[i]) = encode8(f, sc);
+            *reinterpret_cast<uint2*>(q + off[i]) = encode8(f, sc, amax);
         }
         if (tid == 0) s[b] = sc;
         __syncthreads();  // red[] is reused by the next block
