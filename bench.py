@@ -108,6 +108,22 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(mhz)}
 
 
+# ------------------------------------------------------------ multi-rank
+def max_over_ranks(seconds: float, dist=None, device=None) -> float:
+    """The job time of one timed region: the slowest rank's time (every
+    rank runs its own replica; no data moves between ranks)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return seconds
+    t = torch.tensor([seconds], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, flops_per_step: float, steps: int, seconds: float) -> float:
+    """Whole-job TFLOP/s: the work of all ranks over the slowest rank's time."""
+    return world * flops_per_step * steps / seconds / 1e12
+
+
 # ---------------------------------------------------------------- workloads
 def make_workload(config: int, device):
     from fp8_fine_grained_25_b300 import workloads
@@ -287,11 +303,7 @@ def main():
         torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
-    elapsed = start.elapsed_time(stop) / 1e3
-    if dist is not None:
-        t = torch.tensor([elapsed], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed = float(t.item())
+    elapsed = max_over_ranks(start.elapsed_time(stop) / 1e3, dist, device)
     status = path.fp8q.fp8q_get_device_status()
 
     # per-kernel averages from the events around each launch
@@ -334,7 +346,7 @@ def main():
         roofline["hbm_frac"] = roofline["hbm_GB/s"] / peaks["hbm_gbs"]
 
     ms_per_step = elapsed / args.steps * 1e3
-    value = world * flops * args.steps / elapsed / 1e12
+    value = job_throughput(world, flops, args.steps, elapsed)
 
     # end to end through the public API: pinned host inputs in, C back out
     e2e = None
@@ -361,12 +373,8 @@ def main():
             e2e_step()
         s1.record(stream)
         torch.cuda.synchronize()
-        te = s0.elapsed_time(s1) / 1e3
-        if dist is not None:
-            t = torch.tensor([te], device=device)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            te = float(t.item())
-        e2e = {"value": world * flops * args.e2e_steps / te / 1e12, "unit": "TFLOP/s",
+        te = max_over_ranks(s0.elapsed_time(s1) / 1e3, dist, device)
+        e2e = {"value": job_throughput(world, flops, args.e2e_steps, te), "unit": "TFLOP/s",
                "h2d_bytes_per_step": hostA.numel() * 2 + sum(v.numel() * 2 for v in hostW.values()),
                "d2h_bytes_per_step": sum(v.numel() * 2 for v in hostC.values()),
                "ms_per_step": te / args.e2e_steps * 1e3}

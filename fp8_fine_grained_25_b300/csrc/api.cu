@@ -132,8 +132,12 @@ int fp8q_set_gemm_tile_n(int bn) {
 
 int fp8q_get_device_status(cudaStream_t stream, uint32_t* status_out, int clear) {
     if (!status_out) return FP8Q_ERR_NULL;
-    return fp8q::read_device_status(stream, status_out, clear != 0) == cudaSuccess ? FP8Q_OK
-                                                                                  : FP8Q_ERR_CUDA;
+    uint32_t gemm_status = 0, quant_status = 0;
+    if (fp8q::read_device_status(stream, &gemm_status, clear != 0) != cudaSuccess ||
+        fp8q::read_quant_status(&quant_status, clear != 0) != cudaSuccess)
+        return FP8Q_ERR_CUDA;
+    *status_out = gemm_status | quant_status;
+    return FP8Q_OK;
 }
 
 int fp8q_quant_act(const void* x_bf16, int64_t M, int64_t K, void* q_e4m3, float* scales,
@@ -146,7 +150,8 @@ int fp8q_quant_act(const void* x_bf16, int64_t M, int64_t K, void* q_e4m3, float
     if (M * cdiv(K, 128) > kI32Max) return FP8Q_ERR_SHAPE;
     DeviceInfo* dev = nullptr;
     if (int rc = current_device(&dev)) return rc;
-    return fp8q::launch_quant_act(x_bf16, M, K, q_e4m3, scales, stream, dev->sms) == cudaSuccess
+    return fp8q::launch_quant_act(x_bf16, M, K, q_e4m3, scales, stream, dev->sms, g_timeout_ns) ==
+                   cudaSuccess
                ? FP8Q_OK
                : FP8Q_ERR_CUDA;
 }
@@ -160,7 +165,12 @@ int fp8q_quant_weight(const void* w_bf16, int64_t N, int64_t K, void* q_e4m3, fl
         return FP8Q_ERR_ALIGN;
     DeviceInfo* dev = nullptr;
     if (int rc = current_device(&dev)) return rc;
-    return fp8q::launch_quant_weight(w_bf16, N, K, q_e4m3, scales, stream, dev->sms) == cudaSuccess
+    CUtensorMap tmW;
+    if (!make_map_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w_bf16, K, N, 128, 128,
+                     CU_TENSOR_MAP_SWIZZLE_NONE))
+        return FP8Q_ERR_CUDA;
+    return fp8q::launch_quant_weight(&tmW, q_e4m3, scales, N, K, stream, dev->sms, g_timeout_ns) ==
+                   cudaSuccess
                ? FP8Q_OK
                : FP8Q_ERR_CUDA;
 }

@@ -3,9 +3,10 @@
 // item "细粒度量化", Fig. 7a; developer.aliyun.com/article/1776647 §4.1).
 //
 // Both are HBM-bound streams: 2 bytes read and 1 byte written per element
-// plus one fp32 scale per tile/block. Loads and stores are 16-byte / 8-byte
-// vectors, each half-warp owns one 128-element tile row, and the tile amax
-// is a 4-step xor-shuffle max inside the half-warp.
+// plus one fp32 scale per tile/block. A producer warp streams the input into
+// a ring of shared-memory stages with bulk copies (TMA), so the bytes in
+// flight do not depend on registers; consumer warps read a stage, reduce the
+// amax, encode, and store codes (8-byte vectors) and scales to global memory.
 //
 // Arithmetic per tile (bit-exact with the definition):
 //   amax  = max |x|                 (bf16 -> fp32 is exact, max is exact)
@@ -13,14 +14,19 @@
 //   q_i   = E4M3_rn_satfinite(fl32(x_i / s)),  all-zero tile: s = 0, q = 0
 // The per-element quotient uses the tile's reciprocal and one FMA
 // correction instead of a full divide (see div_by_scale).
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "fp8q.h"
+#include "ptx.cuh"
 #include "quant.cuh"
 
 namespace fp8q {
+
+__device__ uint32_t g_quant_status;
 
 namespace {
 
@@ -33,11 +39,13 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4& v, float (&f)[8]) {
     }
 }
 
-__device__ __forceinline__ float absmax8(const float (&f)[8]) {
-    float m = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
-    return m;
+// max |x| of eight bf16 values as bf16 bits: for finite values with the
+// sign cleared, the bit patterns order like the values.
+__device__ __forceinline__ uint32_t absmax_bits8(const uint4& v) {
+    const uint32_t a = __vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu);
+    const uint32_t b = __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu);
+    const uint32_t c = __vmaxu2(a, b);
+    return max(c & 0xFFFFu, c >> 16);
 }
 
 // Two fp32 values -> two E4M3 codes (round to nearest even, saturating to
@@ -64,13 +72,23 @@ __device__ __forceinline__ float div_by_scale(float x, float s, float r) {
 
 constexpr float kFastDivMinAmax = 0x1p-90f;
 
-// Eight values divided by the tile scale and encoded, low byte first.
-// `amax` is the tile's absolute maximum (s = amax / 448).
-__device__ __forceinline__ uint2 encode8(const float (&f)[8], float s, float amax) {
+// s = amax / 448 rounded to nearest, by the same reciprocal-and-correction
+// steps with the constant RN(1/448); equal to the IEEE quotient for every
+// finite non-negative bf16 amax (checked exhaustively by the test suite).
+__device__ __forceinline__ float tile_scale(float amax) {
+    const float r448 = 1.0f / 448.0f;  // RN(1/448), folded at compile time
+    const float q0 = __fmul_rn(amax, r448);
+    const float e = __fmaf_rn(q0, 448.0f, -amax);
+    return __fmaf_rn(-e, r448, q0);
+}
+
+// Eight values of a tile whose scale s and reciprocal r = RN(1/s) (or 0 for
+// the IEEE-divide range, amax < 2^-90) are known, encoded low byte first.
+__device__ __forceinline__ uint2 encode8_r(const uint4& v, float s, float r, bool fast) {
     if (s == 0.0f) return make_uint2(0u, 0u);
-    float y[8];
-    if (amax >= kFastDivMinAmax) {
-        const float r = __frcp_rn(s);
+    float f[8], y[8];
+    unpack_bf16x8(v, f);
+    if (fast) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) y[i] = div_by_scale(f[i], s, r);
     } else {
@@ -83,143 +101,349 @@ __device__ __forceinline__ uint2 encode8(const float (&f)[8], float s, float ama
     return out;
 }
 
-__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+__device__ __forceinline__ uint4 lds16(uint32_t addr) {
     uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
+                 : "r"(addr));
     return v;
 }
 
-constexpr int kActThreads = 256;
-constexpr int kActUnroll = 4;  // tile pairs per warp per iteration
+// A bounded wait taken by a whole warp (see the GEMM kernel).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          uint64_t limit) {
+    return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, abort_flag, limit));
+}
 
-// One half-warp per 1x128 tile; lane `sub` of the half owns columns
-// [8*sub, 8*sub+8) of the tile. A tile t = (m, kb) covers row m, columns
-// [128*kb, min(K, 128*kb + 128)); its scale goes to s[m * KB + kb].
-__global__ void __launch_bounds__(kActThreads) quant_act_kernel(const uint8_t* __restrict__ x,
-                                                                uint8_t* __restrict__ q,
-                                                                float* __restrict__ s,
-                                                                uint32_t T, uint32_t KB,
-                                                                int64_t K) {
-    const uint32_t lane = threadIdx.x & 31u;
-    const uint32_t half = lane >> 4, sub = lane & 15u;
-    const uint64_t warp = (static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const uint64_t nwarps = (static_cast<uint64_t>(gridDim.x) * blockDim.x) >> 5;
-    for (uint64_t base = warp * (2 * kActUnroll); base < T; base += nwarps * (2 * kActUnroll)) {
-        uint4 v[kActUnroll];
-        int64_t off[kActUnroll];
-        bool live[kActUnroll];
-#pragma unroll
-        for (int u = 0; u < kActUnroll; ++u) {
-            const uint64_t t = base + 2 * u + half;
-            const uint32_t m = static_cast<uint32_t>(t / KB);
-            const uint32_t kb = static_cast<uint32_t>(t - static_cast<uint64_t>(m) * KB);
-            const int64_t col = static_cast<int64_t>(kb) * 128 + 8 * sub;
-            off[u] = static_cast<int64_t>(m) * K + col;
-            live[u] = (t < T) && (col < K);
-            v[u] = live[u] ? ld_stream16(x + 2 * off[u]) : make_uint4(0, 0, 0, 0);
+// ------------------------------------------------------------ activations
+// Tile t = (m, kb) = (t / KB, t % KB) covers row m, columns
+// [128 kb, min(K, 128 kb + 128)). Consecutive tiles are adjacent in memory
+// (the last tile of a row ends where the next row starts), so a run of whole
+// tiles is one contiguous byte range: a chunk of kActChunkTiles tiles is one
+// bulk copy. Four lanes encode one tile (8 tiles per warp): lane `sub` of
+// the group owns the 16-byte chunks (4j + sub + 8 * (group & 1)) mod 16,
+// j = 0..3, of the tile's 256 bytes; the rotation by 8 chunks for odd groups
+// keeps every 8-lane shared-memory phase on distinct banks.
+constexpr int kActConsumerWarps = 16;
+constexpr int kActChunkTiles = 8 * kActConsumerWarps;  // 128 tiles, 32 KB of bf16 at most
+constexpr int kActStages = 4;
+constexpr int kActStageBytes = kActChunkTiles * 256;
+constexpr int kActThreads = 32 * (1 + kActConsumerWarps);
+constexpr int kActSmem = kActStages * kActStageBytes + 8 * (2 * kActStages) + 16 + 1024;
+
+struct ActArgs {
+    const uint8_t* x;  // bf16 [M, K]
+    uint8_t* q;        // [M, K]
+    float* s;          // [M, KB]
+    int64_t K;
+    uint32_t T, KB;
+    uint32_t nchunks;
+    uint64_t timeout_ns;
+};
+
+__device__ __forceinline__ int64_t tile_start(int64_t t, uint32_t KB, int64_t K) {
+    const int64_t m = t / KB;
+    return m * K + (t - m * KB) * 128;
+}
+
+template <bool FLAT>  // FLAT: K % 128 == 0, tile t starts at element 128 t
+__global__ void __launch_bounds__(kActThreads, 1) quant_act_kernel(const ActArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sbase = raw + ((1024u - (raw & 1023u)) & 1023u);
+    const uint32_t bar_base = sbase + kActStages * kActStageBytes;
+    auto full = [&](int s) { return bar_base + 8u * s; };
+    auto empty = [&](int s) { return bar_base + 8u * (kActStages + s); };
+    volatile int* abort_flag =
+        reinterpret_cast<volatile int*>(smem_raw + (bar_base - raw) + 8 * 2 * kActStages);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kActStages; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), kActConsumerWarps);
         }
+        *abort_flag = 0;
+        fence_barrier_init();
+        fence_proxy_async_smem();
+    }
+    __syncthreads();
+
+    if (warp == 0) {
+        // producer: one bulk copy per chunk of whole tiles
+        int stage = 0;
+        uint32_t phase = 0, issued = 0;
+        for (uint32_t c = blockIdx.x; c < a.nchunks; c += gridDim.x) {
+            if (!warp_wait(empty(stage), phase ^ 1u, abort_flag, a.timeout_ns)) break;
+            const uint64_t t0 = static_cast<uint64_t>(c) * kActChunkTiles;
+            const uint64_t t1 = t0 + kActChunkTiles < a.T ? t0 + kActChunkTiles : a.T;
+            int64_t b0, b1;
+            if constexpr (FLAT) {
+                b0 = static_cast<int64_t>(t0) * 128;
+                b1 = static_cast<int64_t>(t1) * 128;
+            } else {
+                b0 = tile_start(t0, a.KB, a.K);
+                const int64_t last = t1 - 1, m = last / a.KB;
+                b1 = min(m * a.K + (last - m * a.KB) * 128 + 128, (m + 1) * a.K);
+            }
+            if (elect_one()) {
+                const uint32_t bytes = static_cast<uint32_t>(2 * (b1 - b0));
+                mbar_arrive_expect_tx(full(stage), bytes);
+                bulk_load_1d(sbase + stage * kActStageBytes, a.x + 2 * b0, bytes, full(stage));
+            }
+            __syncwarp();
+            ++issued;
+            if (++stage == kActStages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        for (int s = 0; s < kActStages; ++s) {  // copies in flight land before exit
+            if (static_cast<uint32_t>(s) >= issued) break;
+            const uint32_t last = s + kActStages * ((issued - 1 - s) / kActStages);
+            volatile int local_flag = 0;
+            mbar_wait(full(s), (last / kActStages) & 1u, &local_flag, a.timeout_ns);
+        }
+    } else {
+        const int cw = warp - 1;
+        const uint32_t grp = lane >> 2, sub = lane & 3u;
+        const uint32_t rot = (grp & 1u) * 8u;
+        int stage = 0;
+        uint32_t phase = 0;
+        for (uint32_t c = blockIdx.x; c < a.nchunks; c += gridDim.x) {
+            if (!warp_wait(full(stage), phase, abort_flag, a.timeout_ns)) break;
+            const uint64_t t0 = static_cast<uint64_t>(c) * kActChunkTiles;
+            const int64_t b0 = FLAT ? static_cast<int64_t>(t0) * 128 : tile_start(t0, a.KB, a.K);
+            const uint64_t t = t0 + 8 * cw + grp;  // this group's tile
+            const bool live = t < a.T;
+            int64_t base;   // element offset of the tile in x / q
+            int64_t len;    // elements in the tile (128, less for a K tail)
+            if constexpr (FLAT) {
+                base = static_cast<int64_t>(t) * 128;
+                len = 128;
+            } else {
+                const int64_t m = static_cast<int64_t>(t / a.KB);
+                const int64_t col = (static_cast<int64_t>(t) - m * a.KB) * 128;
+                base = m * a.K + col;
+                len = a.K - col < 128 ? a.K - col : 128;
+            }
+            const uint32_t st = sbase + stage * kActStageBytes + static_cast<uint32_t>(2 * (base - b0));
+            uint4 v[4];
+            uint32_t chunk[4];
 #pragma unroll
-        for (int u = 0; u < kActUnroll; ++u) {
-            float f[8];
-            unpack_bf16x8(v[u], f);
-            float amax = absmax8(f);
+            for (int j = 0; j < 4; ++j) {
+                chunk[j] = (4u * j + sub + rot) & 15u;
+                v[j] = (live && 8 * chunk[j] < len) ? lds16(st + 16u * chunk[j]) : make_uint4(0, 0, 0, 0);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty(stage));  // the stage is in registers now
+            uint32_t bits = max(max(absmax_bits8(v[0]), absmax_bits8(v[1])),
+                                max(absmax_bits8(v[2]), absmax_bits8(v[3])));
+            bits = max(bits, __shfl_xor_sync(0xFFFFFFFFu, bits, 1));
+            bits = max(bits, __shfl_xor_sync(0xFFFFFFFFu, bits, 2));
+            const float amax = __uint_as_float(bits << 16);
+            const float sc = tile_scale(amax);
+            const bool fast = amax >= kFastDivMinAmax;
+            const float r = fast ? __frcp_rn(sc) : 0.0f;
+            if (live) {
 #pragma unroll
-            for (int d = 8; d >= 1; d >>= 1)
-                amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, d));
-            const float sc = __fdiv_rn(amax, 448.0f);
-            const uint64_t t = base + 2 * u + half;
-            if (live[u]) {
-                *reinterpret_cast<uint2*>(q + off[u]) = encode8(f, sc, amax);
-                if (sub == 0) s[t] = sc;
+                for (int j = 0; j < 4; ++j)
+                    if (8 * chunk[j] < len)
+                        *reinterpret_cast<uint2*>(a.q + base + 8 * chunk[j]) = encode8_r(v[j], sc, r, fast);
+                if (sub == 0) a.s[t] = sc;
+            }
+            if (++stage == kActStages) {
+                stage = 0;
+                phase ^= 1u;
             }
         }
     }
+    __syncthreads();
+    if (threadIdx.x == 0 && *abort_flag) atomicOr(&g_quant_status, FP8Q_DEVSTATUS_TIMEOUT);
 }
 
-constexpr int kWThreads = 256;
-constexpr int kWChunks = 8;  // 16-byte chunks per thread: 128 rows x 16 chunks / 256
+// ---------------------------------------------------------------- weights
+// One 128x128 block per stage, loaded as one 2-D TMA box (zero fill past the
+// N and K edges). Consumer thread i owns the 16-byte chunks c = i + 512 j
+// (j = 0..3): block row c / 16, columns [8 (c % 16), +8).
+constexpr int kWConsumerWarps = 16;
+constexpr int kWChunksPerThread = 2048 / (32 * kWConsumerWarps);
+constexpr int kWStages = 4;
+constexpr int kWStageBytes = 128 * 128 * 2;
+constexpr int kWThreads = 32 * (1 + kWConsumerWarps);
+// barriers: full[S], empty[S], red (the per-block amax exchange)
+constexpr int kWBars = 2 * kWStages + 1;
+constexpr int kWSmem = kWStages * kWStageBytes + 8 * kWBars + 16 + 2 * 4 * kWConsumerWarps + 1024;
 
-// One CTA per 128x128 block (grid-stride). Chunk c = tid + 256 * i covers
-// block row c / 16 and columns [8 * (c % 16), +8).
-__global__ void __launch_bounds__(kWThreads) quant_weight_kernel(const uint8_t* __restrict__ w,
-                                                                 uint8_t* __restrict__ q,
-                                                                 float* __restrict__ s,
-                                                                 int64_t N, int64_t K,
-                                                                 uint32_t NB, uint32_t KB) {
-    __shared__ float red[kWThreads / 32];
-    const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
-    const uint64_t nblocks = static_cast<uint64_t>(NB) * KB;
-    for (uint64_t b = blockIdx.x; b < nblocks; b += gridDim.x) {
-        const uint32_t nb = static_cast<uint32_t>(b / KB);
-        const uint32_t kb = static_cast<uint32_t>(b - static_cast<uint64_t>(nb) * KB);
-        uint4 v[kWChunks];
-        int64_t off[kWChunks];
-        bool live[kWChunks];
-#pragma unroll
-        for (int i = 0; i < kWChunks; ++i) {
-            const uint32_t c = tid + kWThreads * i;
-            const int64_t n = static_cast<int64_t>(nb) * 128 + (c >> 4);
-            const int64_t k = static_cast<int64_t>(kb) * 128 + 8 * (c & 15u);
-            live[i] = (n < N) && (k < K);
-            off[i] = n * K + k;
-            v[i] = live[i] ? ld_stream16(w + 2 * off[i]) : make_uint4(0, 0, 0, 0);
+struct WeightArgs {
+    uint8_t* q;  // [N, K]
+    float* s;    // [NB, KB]
+    int64_t N, K;
+    uint32_t NB, KB;
+    uint64_t timeout_ns;
+};
+
+__global__ void __launch_bounds__(kWThreads, 1)
+    quant_weight_kernel(const __grid_constant__ CUtensorMap tmW, const WeightArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+    const uint32_t sbase = raw + pad;
+    const uint32_t bar_base = sbase + kWStages * kWStageBytes;
+    auto full = [&](int s) { return bar_base + 8u * s; };
+    auto empty = [&](int s) { return bar_base + 8u * (kWStages + s); };
+    const uint32_t red_bar = bar_base + 8u * (2 * kWStages);
+    uint8_t* misc = smem_raw + pad + kWStages * kWStageBytes + 8 * kWBars;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(misc);
+    float* red = reinterpret_cast<float*>(misc + 16);  // [2][kWConsumerWarps]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint64_t nblocks = static_cast<uint64_t>(a.NB) * a.KB;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kWStages; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), kWConsumerWarps);
         }
-        float amax = 0.0f;
-#pragma unroll
-        for (int i = 0; i < kWChunks; ++i) {
-            float f[8];
-            unpack_bf16x8(v[i], f);
-            amax = fmaxf(amax, absmax8(f));
-        }
-#pragma unroll
-        for (int d = 16; d >= 1; d >>= 1)
-            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, d));
-        if (lane == 0) red[warp] = amax;
-        __syncthreads();
-        amax = red[0];
-#pragma unroll
-        for (int i = 1; i < kWThreads / 32; ++i) amax = fmaxf(amax, red[i]);
-        const float sc = __fdiv_rn(amax, 448.0f);
-#pragma unroll
-        for (int i = 0; i < kWChunks; ++i) {
-            if (!live[i]) continue;
-            float f[8];
-            unpack_bf16x8(v[i], f);
-            *reinterpret_cast<uint2*>(q + off[i]) = encode8(f, sc, amax);
-        }
-        if (tid == 0) s[b] = sc;
-        __syncthreads();  // red[] is reused by the next block
+        mbar_init(red_bar, kWConsumerWarps);
+        *abort_flag = 0;
+        fence_barrier_init();
+        fence_proxy_async_smem();
     }
+    if (warp == 0 && lane == 0) prefetch_tmap(&tmW);
+    __syncthreads();
+
+    if (warp == 0) {
+        int stage = 0;
+        uint32_t phase = 0, issued = 0;
+        for (uint64_t b = blockIdx.x; b < nblocks; b += gridDim.x) {
+            if (!warp_wait(empty(stage), phase ^ 1u, abort_flag, a.timeout_ns)) break;
+            const uint32_t nb = static_cast<uint32_t>(b / a.KB);
+            const uint32_t kb = static_cast<uint32_t>(b - static_cast<uint64_t>(nb) * a.KB);
+            if (elect_one()) {
+                mbar_arrive_expect_tx(full(stage), kWStageBytes);
+                tma_load_2d(sbase + stage * kWStageBytes, &tmW, full(stage), kb * 128, nb * 128);
+            }
+            __syncwarp();
+            ++issued;
+            if (++stage == kWStages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        for (int s = 0; s < kWStages; ++s) {
+            if (static_cast<uint32_t>(s) >= issued) break;
+            const uint32_t last = s + kWStages * ((issued - 1 - s) / kWStages);
+            volatile int local_flag = 0;
+            mbar_wait(full(s), (last / kWStages) & 1u, &local_flag, a.timeout_ns);
+        }
+    } else {
+        const int cw = warp - 1;
+        const uint32_t tid = threadIdx.x - 32;
+        int stage = 0;
+        uint32_t phase = 0, iter = 0;
+        for (uint64_t b = blockIdx.x; b < nblocks; b += gridDim.x, ++iter) {
+            if (!warp_wait(full(stage), phase, abort_flag, a.timeout_ns)) break;
+            const uint32_t nb = static_cast<uint32_t>(b / a.KB);
+            const uint32_t kb = static_cast<uint32_t>(b - static_cast<uint64_t>(nb) * a.KB);
+            const uint32_t st = sbase + stage * kWStageBytes;
+            constexpr uint32_t kStride = 32 * kWConsumerWarps;
+            uint4 v[kWChunksPerThread];
+#pragma unroll
+            for (int j = 0; j < kWChunksPerThread; ++j) v[j] = lds16(st + 16u * (tid + kStride * j));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty(stage));
+            uint32_t bits = 0;
+#pragma unroll
+            for (int j = 0; j < kWChunksPerThread; ++j) bits = max(bits, absmax_bits8(v[j]));
+#pragma unroll
+            for (int d = 16; d >= 1; d >>= 1) bits = max(bits, __shfl_xor_sync(0xFFFFFFFFu, bits, d));
+            // Block amax across the consumer warps: each publishes its partial
+            // in one half of red[] (alternating per block, so a warp that is a
+            // block ahead never overwrites values still being read) and arrives
+            // on red_bar; the phase of block `iter` has parity iter & 1.
+            float* rb = red + (iter & 1u) * kWConsumerWarps;
+            if (lane == 0) {
+                rb[cw] = __uint_as_float(bits << 16);
+                mbar_arrive(red_bar);
+            }
+            if (!warp_wait(red_bar, iter & 1u, abort_flag, a.timeout_ns)) break;
+            float amax = rb[0];
+#pragma unroll
+            for (int i = 1; i < kWConsumerWarps; ++i) amax = fmaxf(amax, rb[i]);
+            const float sc = tile_scale(amax);
+            const bool fast = amax >= kFastDivMinAmax;
+            const float r = fast ? __frcp_rn(sc) : 0.0f;
+            const int64_t k = static_cast<int64_t>(kb) * 128 + 8 * (tid & 15u);
+            const int64_t n0 = static_cast<int64_t>(nb) * 128 + (tid >> 4);
+#pragma unroll
+            for (int j = 0; j < kWChunksPerThread; ++j) {
+                const int64_t n = n0 + (kStride / 16) * j;
+                if (n < a.N && k < a.K)
+                    *reinterpret_cast<uint2*>(a.q + n * a.K + k) = encode8_r(v[j], sc, r, fast);
+            }
+            if (tid == 0) a.s[b] = sc;
+            if (++stage == kWStages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && *abort_flag) atomicOr(&g_quant_status, FP8Q_DEVSTATUS_TIMEOUT);
 }
 
 }  // namespace
 
 cudaError_t launch_quant_act(const void* x, int64_t M, int64_t K, void* q, float* s,
-                             cudaStream_t stream, int num_sms) {
-    const int64_t KB = (K + 127) / 128;
-    const uint64_t T = static_cast<uint64_t>(M) * KB;
-    const uint64_t per_block = (kActThreads / 32) * 2 * kActUnroll;  // tiles per block-iteration
-    uint64_t want = (T + per_block - 1) / per_block;
-    const uint64_t cap = static_cast<uint64_t>(num_sms) * (2048 / kActThreads);
-    const unsigned grid = static_cast<unsigned>(want < cap ? (want ? want : 1) : cap);
-    quant_act_kernel<<<grid, kActThreads, 0, stream>>>(
-        static_cast<const uint8_t*>(x), static_cast<uint8_t*>(q), s, static_cast<uint32_t>(T),
-        static_cast<uint32_t>(KB), K);
+                             cudaStream_t stream, int num_sms, uint64_t timeout_ns) {
+    ActArgs a;
+    a.x = static_cast<const uint8_t*>(x);
+    a.q = static_cast<uint8_t*>(q);
+    a.s = s;
+    a.K = K;
+    a.KB = static_cast<uint32_t>((K + 127) / 128);
+    a.T = static_cast<uint32_t>(M * a.KB);
+    a.nchunks = (a.T + kActChunkTiles - 1) / kActChunkTiles;
+    a.timeout_ns = timeout_ns;
+    const unsigned grid = a.nchunks < static_cast<uint32_t>(num_sms) ? a.nchunks : num_sms;
+    if (K % 128 == 0) {
+        cudaError_t err = cudaFuncSetAttribute(quant_act_kernel<true>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, kActSmem);
+        if (err != cudaSuccess) return err;
+        quant_act_kernel<true><<<grid, kActThreads, kActSmem, stream>>>(a);
+    } else {
+        cudaError_t err = cudaFuncSetAttribute(quant_act_kernel<false>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, kActSmem);
+        if (err != cudaSuccess) return err;
+        quant_act_kernel<false><<<grid, kActThreads, kActSmem, stream>>>(a);
+    }
     return cudaGetLastError();
 }
 
-cudaError_t launch_quant_weight(const void* w, int64_t N, int64_t K, void* q, float* s,
-                                cudaStream_t stream, int num_sms) {
-    const int64_t KB = (K + 127) / 128, NB = (N + 127) / 128;
-    const uint64_t nblocks = static_cast<uint64_t>(NB) * KB;
-    const uint64_t cap = static_cast<uint64_t>(num_sms) * (2048 / kWThreads);
-    const unsigned grid = static_cast<unsigned>(nblocks < cap ? nblocks : cap);
-    quant_weight_kernel<<<grid, kWThreads, 0, stream>>>(
-        static_cast<const uint8_t*>(w), static_cast<uint8_t*>(q), s, N, K,
-        static_cast<uint32_t>(NB), static_cast<uint32_t>(KB));
+cudaError_t launch_quant_weight(const CUtensorMap* tmW, void* q, float* s, int64_t N, int64_t K,
+                                cudaStream_t stream, int num_sms, uint64_t timeout_ns) {
+    WeightArgs a;
+    a.q = static_cast<uint8_t*>(q);
+    a.s = s;
+    a.N = N;
+    a.K = K;
+    a.NB = static_cast<uint32_t>((N + 127) / 128);
+    a.KB = static_cast<uint32_t>((K + 127) / 128);
+    a.timeout_ns = timeout_ns;
+    const uint64_t nblocks = static_cast<uint64_t>(a.NB) * a.KB;
+    const unsigned grid = static_cast<unsigned>(nblocks < static_cast<uint64_t>(num_sms) ? nblocks : num_sms);
+    cudaError_t err =
+        cudaFuncSetAttribute(quant_weight_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kWSmem);
+    if (err != cudaSuccess) return err;
+    quant_weight_kernel<<<grid, kWThreads, kWSmem, stream>>>(*tmW, a);
     return cudaGetLastError();
+}
+
+cudaError_t read_quant_status(uint32_t* out, bool clear) {
+    cudaError_t err = cudaMemcpyFromSymbol(out, g_quant_status, sizeof(uint32_t));
+    if (err != cudaSuccess || !clear) return err;
+    const uint32_t zero = 0;
+    return cudaMemcpyToSymbol(g_quant_status, &zero, sizeof(uint32_t));
 }
 
 }  // namespace fp8q

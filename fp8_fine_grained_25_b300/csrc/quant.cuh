@@ -1,14 +1,17 @@
 // Internal interface between the C-ABI layer and the quantizer kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 namespace fp8q {
 
 cudaError_t launch_quant_act(const void* x, int64_t M, int64_t K, void* q, float* s,
-                             cudaStream_t stream, int num_sms);
-cudaError_t launch_quant_weight(const void* w, int64_t N, int64_t K, void* q, float* s,
-                                cudaStream_t stream, int num_sms);
+                             cudaStream_t stream, int num_sms, uint64_t timeout_ns);
+// tmW: bf16 [N, K] tensor map, box 128 x 128, no swizzle
+cudaError_t launch_quant_weight(const CUtensorMap* tmW, void* q, float* s, int64_t N, int64_t K,
+                                cudaStream_t stream, int num_sms, uint64_t timeout_ns);
+cudaError_t read_quant_status(uint32_t* out, bool clear);
 
 }  // namespace fp8q

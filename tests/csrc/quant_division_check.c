@@ -9,7 +9,10 @@
  * this program checks that q equals the IEEE quotient bit for bit whenever
  * |x / s| >= 2^-12, and that smaller quotients keep the IEEE sign and stay
  * below 2^-11 (every such value encodes to the same signed E4M3 zero).
- * Prints "pairs mismatches" and exits 0.
+ * It also checks the tile scale s = amax / 448, computed the same way with
+ * the constant reciprocal RN(1/448), against the IEEE quotient for every
+ * finite non-negative bf16 amax.
+ * Prints "pairs mismatches scale_mismatches" and exits 0.
  */
 #include <math.h>
 #include <stdint.h>
@@ -54,6 +57,15 @@ int main(void) {
             }
         }
     }
-    printf("%lld %lld\n", pairs, bad);
+    long long scale_bad = 0;
+    const float r448 = 1.0f / 448.0f;
+    for (uint32_t ab = 0; ab < 0x7F80; ++ab) {
+        const float amax = bf16_to_f32(ab);
+        const float q0 = amax * r448;
+        const float e = fmaf(q0, 448.0f, -amax);
+        const float s = fmaf(-e, r448, q0);
+        if (bits(s) != bits(amax / 448.0f)) ++scale_bad;
+    }
+    printf("%lld %lld %lld\n", pairs, bad, scale_bad);
     return 0;
 }
