@@ -22,6 +22,7 @@ struct DeviceInfo {
     bool init = false;
     bool supported = false;
     int sms = 0;
+    int pair_clusters = -1;  // co-resident 2-CTA clusters of the pair kernel (-1: not queried)
 };
 
 constexpr int kMaxDevices = 64;
@@ -29,6 +30,7 @@ DeviceInfo g_devices[kMaxDevices];
 std::mutex g_mutex;
 uint64_t g_timeout_ns = 1000000000ull;
 int g_force_bn = 0;
+int g_pair_mode = 1;  // 1: use 2-CTA pairs for the dense GEMM where they fit
 constexpr int64_t kI32Max = 2147483647;
 
 int current_device(DeviceInfo** out) {
@@ -130,6 +132,11 @@ int fp8q_set_gemm_tile_n(int bn) {
     return FP8Q_OK;
 }
 
+int fp8q_set_gemm_pairs(int enable) {
+    g_pair_mode = enable ? 1 : 0;
+    return FP8Q_OK;
+}
+
 int fp8q_get_device_status(cudaStream_t stream, uint32_t* status_out, int clear) {
     if (!status_out) return FP8Q_ERR_NULL;
     uint32_t gemm_status = 0, quant_status = 0;
@@ -188,9 +195,17 @@ int fp8_block_gemm(const void* A, const float* sa, const void* B, const float* s
     if (int rc = current_device(&dev)) return rc;
 
     const int bn = g_force_bn ? g_force_bn : choose_bn(M, N, dev->sms);
+    // 2-CTA pairs (256 x 256 tiles over two SMs) for the 256-wide tile when
+    // there are at least two m-tiles to pair.
+    bool pair = g_pair_mode && bn == 256 && M > 128;
+    if (pair) {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        if (dev->pair_clusters < 0) dev->pair_clusters = fp8q::gemm_pair_max_clusters(256);
+        pair = dev->pair_clusters > 0;
+    }
     CUtensorMap tmA, tmB, tmC;
     if (!make_map_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, K, M, 128, 128) ||
-        !make_map_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, K, N, 128, bn) ||
+        !make_map_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, K, N, 128, pair ? bn / 2 : bn) ||
         !make_map_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C_bf16, N, M, 32, 32,
                      CU_TENSOR_MAP_SWIZZLE_64B))
         return FP8Q_ERR_CUDA;
@@ -201,6 +216,7 @@ int fp8_block_gemm(const void* A, const float* sa, const void* B, const float* s
     g.tmC = &tmC;
     g.bn = bn;
     g.grouped = false;
+    g.pair = pair;
     g.stream = stream;
     fp8q::GemmArgs& a = g.args;
     a.sa = sa;
@@ -215,12 +231,19 @@ int fp8_block_gemm(const void* A, const float* sa, const void* B, const float* s
     a.E = 1;
     a.mt_count = static_cast<int32_t>(cdiv(M, 128));
     a.nt_count = static_cast<int32_t>(cdiv(N, bn));
-    const int64_t tiles = static_cast<int64_t>(a.mt_count) * a.nt_count;
-    if (tiles > kI32Max) return FP8Q_ERR_SHAPE;
-    a.num_tiles = static_cast<int32_t>(tiles);
+    a.mp_count = static_cast<int32_t>(cdiv(a.mt_count, 2));
+    // work units: tiles, or pairs of m-tiles in pair mode
+    const int64_t units = static_cast<int64_t>(pair ? a.mp_count : a.mt_count) * a.nt_count;
+    if (units > kI32Max) return FP8Q_ERR_SHAPE;
+    a.num_tiles = static_cast<int32_t>(units);
     a.timeout_ns = g_timeout_ns;
     a.debug = 0;
-    g.grid = static_cast<unsigned>(tiles < dev->sms ? tiles : dev->sms);
+    if (pair) {
+        const int64_t clusters = units < dev->pair_clusters ? units : dev->pair_clusters;
+        g.grid = static_cast<unsigned>(2 * clusters);
+    } else {
+        g.grid = static_cast<unsigned>(units < dev->sms ? units : dev->sms);
+    }
     return fp8q::launch_gemm(g) == cudaSuccess ? FP8Q_OK : FP8Q_ERR_CUDA;
 }
 
@@ -252,6 +275,7 @@ int fp8_grouped_gemm(const void* A, const float* sa, const void* B, const float*
     g.tmC = &tmA;  // unused: the grouped epilogue stores directly
     g.bn = bn;
     g.grouped = true;
+    g.pair = false;
     g.stream = stream;
     fp8q::GemmArgs& a = g.args;
     a.sa = sa;
@@ -265,6 +289,7 @@ int fp8_grouped_gemm(const void* A, const float* sa, const void* B, const float*
     a.NB = static_cast<int32_t>(cdiv(N, 128));
     a.E = E;
     a.mt_count = 0;
+    a.mp_count = 0;
     a.nt_count = static_cast<int32_t>(cdiv(N, bn));
     // Upper bound of the tile count (sum over experts of ceil(rows/128) *
     // n-tiles) must fit the kernel's int32 tile ids.

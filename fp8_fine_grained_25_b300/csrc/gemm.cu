@@ -12,9 +12,10 @@
 //               accumulate per K block), then commit to the stage's "empty"
 //               barrier and the buffer's "full" barrier. Allocates and frees
 //               TMEM. The warp stays converged and one elected lane issues.
-//   warp 2      scale loader: per K block, cp.async copies of sa[m0..m0+127][kb]
-//               and the tile's sb[nb][kb] into a shared-memory scale ring, so
-//               the promotion never waits on a global load.
+//   warp 2      scale loader: per group of 4 K blocks, cp.async copies of
+//               sa[m0..m0+127][kb..kb+3] and the tile's sb[nb][kb..kb+3] into a
+//               shared-memory scale ring, so the promotion never waits on a
+//               global load and touches the ring once per 4 K blocks.
 //   warps 4-11  promotion + epilogue: tcgen05.ld P_kb (each warp owns 32
 //               TMEM lanes = 32 rows and half of the BN columns), then
 //               acc += P_kb * (sa[m][kb] * sb[n/128][kb]) with packed FP32
@@ -25,6 +26,16 @@
 // Several TMEM buffers let the MMA of later K blocks overlap the promotion
 // of earlier ones. Every wait is bounded in time; on expiry the CTA raises
 // an abort flag, drains its copies and MMAs, frees TMEM and returns.
+//
+// Pair mode (dense GEMM): two CTAs of a cluster compute a 256 x BN tile with
+// the 2-CTA MMA (tcgen05 cta_group::2). Each CTA holds its own 128 rows of A
+// and half of the tile's B rows, so each SM's shared memory carries 32 KB
+// of operands per K block instead of 48 KB (TMA writes plus MMA reads are
+// the shared-memory bandwidth bound of the one-CTA tile). The even CTA
+// issues the MMAs; both CTAs' loads count on its "full" barrier, both CTAs'
+// promotion warps release its TMEM barrier, and its commits arrive on the
+// "empty"/"full" barriers of both CTAs. Each CTA promotes and stores the
+// 128 x BN accumulator in its own tensor memory.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -49,17 +60,20 @@ constexpr int kEpiWarps = 8;
 constexpr int kGroupM = 16;     // rasterisation: m-tiles per group for L2 reuse
 constexpr int kSmemLimit = 232448;
 constexpr int kCtrlRegs = 40, kEpiRegs = 232;  // setmaxnreg split: 128*40 + 256*232 = 384*168
-constexpr int kScaleSlots = 8;  // K blocks of scales staged ahead
-constexpr int kMaxNb = 4;       // 128-column blocks one tile can touch (BN <= 256: at most 3)
+constexpr int kScaleKb = 4;     // K blocks of scales per ring slot
+constexpr int kScaleSlots = 4;  // ring slots (16 K blocks staged ahead)
+constexpr int kMaxNb = 2;       // 128-column blocks of one tile (BN <= 256, n0 % BN == 0)
 
-template <int BN, bool GROUPED>
+template <int BN, bool GROUPED, bool PAIR>
 struct Layout {
     static constexpr int A_BYTES = BM * BK;
-    static constexpr int B_BYTES = BN * BK;
+    static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // rows of B this CTA loads
+    static constexpr int B_BYTES = B_ROWS * BK;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int EPI_WARP_BYTES = 32 * 32 * 2;  // 32 rows x 32 bf16, 64-byte swizzle
     static constexpr int EPI_BYTES = GROUPED ? 0 : kEpiWarps * EPI_WARP_BYTES;
-    static constexpr int SCALE_SLOT_BYTES = 4 * (BM + kMaxNb);  // sa[128] then sb[kMaxNb]
+    // slot: sa as [128 rows][kScaleKb], then sb as [kMaxNb][kScaleKb]
+    static constexpr int SCALE_SLOT_BYTES = 4 * kScaleKb * (BM + kMaxNb);
     static constexpr int SCALE_BYTES = kScaleSlots * SCALE_SLOT_BYTES;
     static constexpr int NBUF = (512 / BN) > 4 ? 4 : (512 / BN);  // TMEM buffers of BN columns
     static constexpr int TMEM_COLS = NBUF * BN <= 128 ? 128 : NBUF * BN <= 256 ? 256 : 512;
@@ -81,6 +95,7 @@ struct Layout {
     static constexpr int HALF = BN / 2;       // columns per promotion warp
     static constexpr int CHUNKS = HALF / 32;  // 32-column TMEM loads, issued in pairs
     static_assert(BN == 128 || BN == 256, "tile width must be 128 or 256");
+    static_assert(!(PAIR && GROUPED), "pair mode is for the dense GEMM");
     static_assert(STAGES >= 2, "not enough shared memory for two stages");
     static_assert(8 * NUM_BARS + 16 <= 512, "barrier area overflow");
     static constexpr int smem_bytes(int E) {
@@ -101,19 +116,25 @@ struct Tile {
     int e;        // expert (0 when dense)
 };
 
-template <int BN, bool GROUPED>
-__device__ __forceinline__ Tile decode_tile(const GemmArgs& a, const int* table, int t) {
+// Work unit t -> tile. Dense: groups of kGroupM row-units share n-tiles
+// for L2 reuse. Pair mode: a unit is a pair of m-tiles (2u, 2u + 1), CTA
+// `rank` of the pair takes m-tile 2u + rank and B rows n0 + rank * BN / 2.
+template <int BN, bool GROUPED, bool PAIR>
+__device__ __forceinline__ Tile decode_tile(const GemmArgs& a, const int* table, int t,
+                                            uint32_t rank) {
     Tile r;
     if constexpr (!GROUPED) {
+        const int rows = PAIR ? a.mp_count : a.mt_count;
         const int per_group = kGroupM * a.nt_count;
         const int g = t / per_group, in = t - g * per_group;
         const int first = g * kGroupM;
-        const int gm = min(kGroupM, a.mt_count - first);
-        const int mt = first + in % gm, nt = in / gm;
+        const int gm = min(kGroupM, rows - first);
+        const int mu = first + in % gm, nt = in / gm;
+        const int mt = PAIR ? 2 * mu + static_cast<int>(rank) : mu;
         r.m0 = mt * BM;
         r.row_end = a.M;
         r.n0 = nt * BN;
-        r.brow = r.n0;
+        r.brow = r.n0 + (PAIR ? static_cast<int>(rank) * (BN / 2) : 0);
         r.e = 0;
     } else {
         int lo = 0, hi = a.E - 1;  // largest e with table[e] <= t
@@ -172,16 +193,17 @@ __device__ void build_group_table(const GemmArgs& a, int* table) {
 
 // A bounded wait taken by a whole warp: true only if every lane saw the
 // phase complete (the lanes may disagree only at the time limit).
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           uint64_t limit) {
-    return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, abort_flag, limit));
+    return __all_sync(0xFFFFFFFFu, mbar_wait<CLUSTER>(bar, parity, abort_flag, limit));
 }
 
-template <int BN, bool GROUPED>
+template <int BN, bool GROUPED, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
-    using L = Layout<BN, GROUPED>;
+    using L = Layout<BN, GROUPED, PAIR>;
     constexpr int S = L::STAGES;
     constexpr int NBUF = L::NBUF;
     extern __shared__ uint8_t smem_raw[];
@@ -198,15 +220,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const uint64_t limit = args.timeout_ns;
+    // Pair mode: rank in the pair; the even CTA owns the MMA-side barriers.
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+    const bool leader = rank == 0;
+    auto lead_bar = [&](int i) -> uint32_t { return PAIR ? mapa_shared(bar(i), 0) : bar(i); };
+    const int unit0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+    const int unit_step = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(bar(L::FULL + s), 1);
+            mbar_init(bar(L::FULL + s), PAIR ? 2 : 1);  // pair: both CTAs' producers
             mbar_init(bar(L::EMPTY + s), 1);
         }
         for (int b = 0; b < NBUF; ++b) {
             mbar_init(bar(L::TFULL + b), 1);
-            mbar_init(bar(L::TEMPTY + b), kEpiWarps);
+            mbar_init(bar(L::TEMPTY + b), PAIR ? 2 * kEpiWarps : kEpiWarps);
         }
         for (int j = 0; j < kScaleSlots; ++j) {
             mbar_init(bar(L::SFULL + j), 32);  // one cp.async completion arrive per lane
@@ -223,14 +251,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (!GROUPED) prefetch_tmap(&tmC);
     }
     if (warp == 1) {
-        tmem_alloc(sbase + L::MISC_OFF, L::TMEM_COLS);
-        tmem_relinquish_alloc_permit();
+        tmem_alloc<PAIR>(sbase + L::MISC_OFF, L::TMEM_COLS);
+        tmem_relinquish_alloc_permit<PAIR>();
     }
     if constexpr (GROUPED) {
         if (warp == 3) build_group_table(args, table);
     }
     tc_fence_before_sync();
     __syncthreads();
+    if constexpr (PAIR) cluster_sync();  // peer barriers initialised before any remote arrive
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
     const int num_tiles = GROUPED ? table[args.E] : args.num_tiles;
@@ -248,8 +277,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             int stage = 0;
             uint32_t phase = 0, issued = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
-                const Tile tile = decode_tile<BN, GROUPED>(args, table, t);
+            for (int t = unit0; ok && t < num_tiles; t += unit_step) {
+                const Tile tile = decode_tile<BN, GROUPED, PAIR>(args, table, t, rank);
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!warp_wait(bar(L::EMPTY + stage), phase ^ 1u, abort_flag, limit)) {
                         ok = false;
@@ -258,10 +287,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (elect_one()) {
                         uint32_t bytes = L::STAGE_BYTES;
                         if ((args.debug & 1u) && issued == 0) bytes += 16;  // never-completing phase
-                        mbar_arrive_expect_tx(bar(L::FULL + stage), bytes);
                         const uint32_t sA = sbase + stage * L::STAGE_BYTES;
-                        tma_load_2d(sA, &tmA, bar(L::FULL + stage), kb * BK, tile.m0);
-                        tma_load_2d(sA + L::A_BYTES, &tmB, bar(L::FULL + stage), kb * BK, tile.brow);
+                        if constexpr (PAIR) {
+                            const uint32_t fb = lead_bar(L::FULL + stage);
+                            mbar_arrive_expect_tx_cluster(fb, bytes);
+                            tma_load_2d_pair(sA, &tmA, fb, kb * BK, tile.m0);
+                            tma_load_2d_pair(sA + L::A_BYTES, &tmB, fb, kb * BK, tile.brow);
+                        } else {
+                            mbar_arrive_expect_tx(bar(L::FULL + stage), bytes);
+                            tma_load_2d(sA, &tmA, bar(L::FULL + stage), kb * BK, tile.m0);
+                            tma_load_2d(sA + L::A_BYTES, &tmB, bar(L::FULL + stage), kb * BK, tile.brow);
+                        }
                     }
                     __syncwarp();
                     ++issued;
@@ -272,23 +308,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             // Wait for the copies still landing in shared memory (normally
-            // all consumed already) before the CTA may exit.
-            for (int s = 0; s < S; ++s) {
+            // all consumed already) before the CTA may exit. In pair mode the
+            // even CTA's full barriers count both CTAs' bytes, and the odd CTA
+            // leaves only after the closing cluster barrier.
+            for (int s = 0; s < S && leader; ++s) {
                 if (static_cast<uint32_t>(s) >= issued) break;
                 const uint32_t last = s + S * ((issued - 1 - s) / S);
                 volatile int local_flag = 0;
                 mbar_wait(bar(L::FULL + s), (last / S) & 1u, &local_flag, limit);
             }
-        } else if (warp == 1) {
+        } else if (warp == 1 && leader) {
             // --------------------------------------------------- MMA issuer
-            constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
+            constexpr uint32_t idesc = idesc_e4m3_f32(PAIR ? 2 * BM : BM, BN);
             int stage = 0;
             uint32_t phase = 0, abuf = 0, aphase = 0;
             bool ok = true, issued_any = false;
-            for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+            for (int t = unit0; ok && t < num_tiles; t += unit_step) {
                 for (int kb = 0; kb < KB; ++kb) {
-                    if (!warp_wait(bar(L::TEMPTY + abuf), aphase ^ 1u, abort_flag, limit) ||
-                        !warp_wait(bar(L::FULL + stage), phase, abort_flag, limit)) {
+                    if (!warp_wait<PAIR>(bar(L::TEMPTY + abuf), aphase ^ 1u, abort_flag, limit) ||
+                        !warp_wait<PAIR>(bar(L::FULL + stage), phase, abort_flag, limit)) {
                         ok = false;
                         break;
                     }
@@ -298,11 +336,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t bd = sdesc_k_sw128(sA + L::A_BYTES);
                     const uint32_t d = tmem_base + abuf * BN;
                     if (elect_one()) {
+                        if constexpr (PAIR) {
 #pragma unroll
-                        for (int k = 0; k < BK / 32; ++k)
-                            mma_e4m3(d, ad + 2u * k, bd + 2u * k, idesc, k > 0 ? 1u : 0u);
-                        mma_commit(bar(L::EMPTY + stage));
-                        mma_commit(bar(L::TFULL + abuf));
+                            for (int k = 0; k < BK / 32; ++k)
+                                mma_e4m3_pair(d, ad + 2u * k, bd + 2u * k, idesc, k > 0 ? 1u : 0u);
+                            mma_commit_pair(bar(L::EMPTY + stage));
+                            mma_commit_pair(bar(L::TFULL + abuf));
+                        } else {
+#pragma unroll
+                            for (int k = 0; k < BK / 32; ++k)
+                                mma_e4m3(d, ad + 2u * k, bd + 2u * k, idesc, k > 0 ? 1u : 0u);
+                            mma_commit(bar(L::EMPTY + stage));
+                            mma_commit(bar(L::TFULL + abuf));
+                        }
                     }
                     __syncwarp();
                     issued_any = true;
@@ -318,26 +364,34 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // Every MMA issued above has completed once this arrives.
             if (issued_any) {
-                if (elect_one()) mma_commit(bar(L::DRAIN));
+                if (elect_one()) {
+                    if constexpr (PAIR) mma_commit_pair_local(bar(L::DRAIN));
+                    else mma_commit(bar(L::DRAIN));
+                }
                 __syncwarp();
                 volatile int local_flag = 0;
                 mbar_wait(bar(L::DRAIN), 0, &local_flag, limit);
             }
         } else if (warp == kScaleWarp) {
             // ------------------------------------------------- scale loader
-            // Slot j holds, for one K block, sa of the tile's 128 rows (row r
-            // at float r) and sb of the tile's 128-column blocks from n0/128
-            // on (at floats 128..131). Rows outside the tile and blocks past
-            // the last one are written as zero.
+            // Slot j holds K blocks [kb0, kb0 + 4): sa of the tile's 128 rows
+            // (row r at floats 4r .. 4r + 3) and sb of the tile's two 128-column
+            // blocks (block i at floats 512 + 4i ..). Rows outside the tile,
+            // blocks past the last one and K blocks past the end are zero.
+            // When KB % 4 == 0 (and sa, sb are 16-byte aligned) each row's four
+            // values are one 16-byte copy.
+            const bool wide = (KB % kScaleKb) == 0 &&
+                              ((reinterpret_cast<uintptr_t>(args.sa) |
+                                reinterpret_cast<uintptr_t>(args.sb)) & 15u) == 0;
             int slot = 0;
             uint32_t sphase = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
-                const Tile tile = decode_tile<BN, GROUPED>(args, table, t);
+            for (int t = unit0; ok && t < num_tiles; t += unit_step) {
+                const Tile tile = decode_tile<BN, GROUPED, PAIR>(args, table, t, rank);
                 const float* sb_e = args.sb + static_cast<int64_t>(tile.e) * args.NB * KB;
-                const int nb = (tile.n0 >> 7) + lane;
+                const int nb = (tile.n0 >> 7) + (lane & (kMaxNb - 1));
                 const bool sb_ok = lane < kMaxNb && nb < args.NB && (nb << 7) < tile.n0 + BN;
-                for (int kb = 0; kb < KB; ++kb) {
+                for (int kb0 = 0; kb0 < KB; kb0 += kScaleKb) {
                     if (!warp_wait(bar(L::SEMPTY + slot), sphase ^ 1u, abort_flag, limit)) {
                         ok = false;
                         break;
@@ -348,12 +402,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int r = lane + 32 * i;
                         const int m = tile.m0 + r;
                         const bool live = m < tile.row_end;
-                        const float* src = args.sa + (live ? static_cast<int64_t>(m) * KB + kb : 0);
-                        cp_async_4(sl + 4u * r, src, live ? 4u : 0u);
+                        const float* src = args.sa + (live ? static_cast<int64_t>(m) * KB + kb0 : 0);
+                        if (wide) {
+                            cp_async_16(sl + 16u * r, src, live ? 16u : 0u);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < kScaleKb; ++j) {
+                                const bool in = live && kb0 + j < KB;
+                                cp_async_4(sl + 16u * r + 4u * j, in ? src + j : args.sa, in ? 4u : 0u);
+                            }
+                        }
                     }
                     if (lane < kMaxNb) {
-                        const float* src = sb_e + (sb_ok ? static_cast<int64_t>(nb) * KB + kb : 0);
-                        cp_async_4(sl + 4u * (BM + lane), src, sb_ok ? 4u : 0u);
+                        const float* src = sb_e + (sb_ok ? static_cast<int64_t>(nb) * KB + kb0 : 0);
+                        const uint32_t dst = sl + 16u * (BM + lane);
+                        if (wide) {
+                            cp_async_16(dst, src, sb_ok ? 16u : 0u);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < kScaleKb; ++j) {
+                                const bool in = sb_ok && kb0 + j < KB;
+                                cp_async_4(dst + 4u * j, in ? src + j : args.sb, in ? 4u : 0u);
+                            }
+                        }
                     }
                     cp_async_mbar_arrive(bar(L::SFULL + slot));
                     if (++slot == kScaleSlots) {
@@ -378,8 +449,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         int slot = 0;
         uint32_t sphase = 0;
         bool ok = true;
-        for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
-            const Tile tile = decode_tile<BN, GROUPED>(args, table, t);
+        const uint32_t temptry_base = PAIR ? mapa_shared(bar(L::TEMPTY), 0) : bar(L::TEMPTY);
+        for (int t = unit0; ok && t < num_tiles; t += unit_step) {
+            const Tile tile = decode_tile<BN, GROUPED, PAIR>(args, table, t, rank);
             const int m = tile.m0 + row;
             const bool row_ok = m < tile.row_end;
             const int col0 = tile.n0 + h * L::HALF;  // first column of this warp
@@ -387,26 +459,33 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < L::HALF; ++j) acc[j] = 0.0f;
 
+            // This warp's columns lie in one 128-column block (n0 % BN == 0),
+            // so each K block needs one scale product sa[m][kb] * sb[nb][kb].
+            const int rel_nb = (h * L::HALF) >> 7;
+            float4 sa4 = make_float4(0.f, 0.f, 0.f, 0.f), sb4 = sa4;
             for (int kb = 0; kb < KB; ++kb) {
-                // scales of this K block, from the ring (staged ahead)
-                if (!warp_wait(bar(L::SFULL + slot), sphase, abort_flag, limit)) {
-                    ok = false;
-                    break;
+                const int j = kb & (kScaleKb - 1);
+                if (j == 0) {
+                    // scales of K blocks kb .. kb + 3, from the ring (staged ahead)
+                    if (!warp_wait(bar(L::SFULL + slot), sphase, abort_flag, limit)) {
+                        ok = false;
+                        break;
+                    }
+                    const float* sl = scale_ring + slot * (L::SCALE_SLOT_BYTES / 4);
+                    sa4 = *reinterpret_cast<const float4*>(sl + 4 * row);
+                    sb4 = *reinterpret_cast<const float4*>(sl + 4 * (BM + rel_nb));
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(L::SEMPTY + slot));
+                    if (++slot == kScaleSlots) {
+                        slot = 0;
+                        sphase ^= 1u;
+                    }
                 }
-                const float* sl = scale_ring + slot * (L::SCALE_SLOT_BYTES / 4);
-                const float a_s = sl[row];
-                float cs[L::CHUNKS];
-#pragma unroll
-                for (int c = 0; c < L::CHUNKS; ++c)
-                    cs[c] = a_s * sl[BM + ((h * L::HALF + 32 * c) >> 7)];
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(L::SEMPTY + slot));
-                if (++slot == kScaleSlots) {
-                    slot = 0;
-                    sphase ^= 1u;
-                }
+                const float a_s = j == 0 ? sa4.x : j == 1 ? sa4.y : j == 2 ? sa4.z : sa4.w;
+                const float b_s = j == 0 ? sb4.x : j == 1 ? sb4.y : j == 2 ? sb4.z : sb4.w;
+                const float cs = a_s * b_s;
 
-                if (!warp_wait(bar(L::TFULL + abuf), aphase, abort_flag, limit)) {
+                if (!warp_wait<PAIR>(bar(L::TFULL + abuf), aphase, abort_flag, limit)) {
                     ok = false;
                     break;
                 }
@@ -419,16 +498,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld32(taddr + 32 * (c + 1), r1);
                     tmem_wait_ld64(r0, r1);
 #pragma unroll
-                    for (int j = 0; j < 32; j += 2)
-                        ffma2(acc[32 * c + j], acc[32 * c + j + 1], r0[j], r0[j + 1], cs[c]);
+                    for (int i = 0; i < 32; i += 2)
+                        ffma2(acc[32 * c + i], acc[32 * c + i + 1], r0[i], r0[i + 1], cs);
 #pragma unroll
-                    for (int j = 0; j < 32; j += 2)
-                        ffma2(acc[32 * (c + 1) + j], acc[32 * (c + 1) + j + 1], r1[j], r1[j + 1],
-                              cs[c + 1]);
+                    for (int i = 0; i < 32; i += 2)
+                        ffma2(acc[32 * (c + 1) + i], acc[32 * (c + 1) + i + 1], r1[i], r1[i + 1], cs);
                 }
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(L::TEMPTY + abuf));
+                if (lane == 0) {
+                    if constexpr (PAIR) mbar_arrive_cluster(temptry_base + 8u * abuf);
+                    else mbar_arrive(bar(L::TEMPTY + abuf));
+                }
                 if (++abuf == NBUF) {
                     abuf = 0;
                     aphase ^= 1u;
@@ -492,17 +573,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before_sync();
     __syncthreads();
+    if constexpr (PAIR) cluster_sync();  // the even CTA's MMAs (drained) may write our TMEM
     if (warp == 1) {
         tc_fence_after_sync();
-        tmem_dealloc(tmem_base, L::TMEM_COLS);
+        tmem_dealloc<PAIR>(tmem_base, L::TMEM_COLS);
     }
     if (threadIdx.x == 0 && *abort_flag) atomicOr(&g_device_status, FP8Q_DEVSTATUS_TIMEOUT);
 }
 
-template <int BN, bool GROUPED>
-cudaError_t launch_one(const GemmLaunch& g) {
-    using L = Layout<BN, GROUPED>;
-    auto kern = fp8_gemm_kernel<BN, GROUPED>;
+template <int BN, bool GROUPED, bool PAIR>
+cudaError_t prepare(int smem) {
+    auto kern = fp8_gemm_kernel<BN, GROUPED, PAIR>;
     // setmaxnreg.inc waits until the registers it asks for are free in the
     // CTA's launch pool; a pool smaller than the split would never satisfy
     // it, so refuse to launch in that case.
@@ -511,33 +592,82 @@ cudaError_t launch_one(const GemmLaunch& g) {
     if (err != cudaSuccess) return err;
     if (fa.numRegs * kThreads < kCtrlRegs * 128 + kEpiRegs * 256 || fa.maxThreadsPerBlock < kThreads)
         return cudaErrorInvalidConfiguration;
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+}
+
+template <int BN, bool GROUPED, bool PAIR>
+cudaError_t launch_one(const GemmLaunch& g) {
+    using L = Layout<BN, GROUPED, PAIR>;
+    auto kern = fp8_gemm_kernel<BN, GROUPED, PAIR>;
     const int smem = L::smem_bytes(GROUPED ? g.args.E : 0);
-    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t err = prepare<BN, GROUPED, PAIR>(smem);
     if (err != cudaSuccess) return err;
-    kern<<<g.grid, kThreads, smem, g.stream>>>(*g.tmA, *g.tmB, *g.tmC, g.args);
-    return cudaGetLastError();
+    if constexpr (!PAIR) {
+        kern<<<g.grid, kThreads, smem, g.stream>>>(*g.tmA, *g.tmB, *g.tmC, g.args);
+        return cudaGetLastError();
+    } else {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(g.grid, 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = g.stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, kern, *g.tmA, *g.tmB, *g.tmC, g.args);
+    }
+}
+
+template <int BN>
+int pair_max_clusters() {
+    using L = Layout<BN, false, true>;
+    const int smem = L::smem_bytes(0);
+    if (prepare<BN, false, true>(smem) != cudaSuccess) return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, fp8_gemm_kernel<BN, false, true>, &cfg) != cudaSuccess)
+        return 0;
+    return n;
 }
 
 }  // namespace
 
 int gemm_stages(int bn) {
     switch (bn) {
-        case 128: return Layout<128, false>::STAGES;
-        case 256: return Layout<256, false>::STAGES;
+        case 128: return Layout<128, false, false>::STAGES;
+        case 256: return Layout<256, false, false>::STAGES;
         default: return 0;
     }
 }
 
+int gemm_pair_max_clusters(int bn) { return bn == 256 ? pair_max_clusters<256>() : 0; }
+
 cudaError_t launch_gemm(const GemmLaunch& g) {
     if (g.grouped) {
         switch (g.bn) {
-            case 128: return launch_one<128, true>(g);
-            case 256: return launch_one<256, true>(g);
+            case 128: return launch_one<128, true, false>(g);
+            case 256: return launch_one<256, true, false>(g);
         }
+    } else if (g.pair) {
+        if (g.bn == 256) return launch_one<256, false, true>(g);
     } else {
         switch (g.bn) {
-            case 128: return launch_one<128, false>(g);
-            case 256: return launch_one<256, false>(g);
+            case 128: return launch_one<128, false, false>(g);
+            case 256: return launch_one<256, false, false>(g);
         }
     }
     return cudaErrorInvalidValue;

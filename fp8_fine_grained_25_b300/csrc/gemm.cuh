@@ -19,6 +19,7 @@ struct GemmArgs {
     int32_t KB, NB;          // ceil(K / 128), ceil(N / 128)
     int32_t E;               // experts (grouped), else 1
     int32_t mt_count, nt_count;
+    int32_t mp_count;        // pair mode: ceil(mt_count / 2) row units
     int32_t num_tiles;       // dense only; the grouped kernel counts its own
     uint64_t timeout_ns;
     uint32_t debug;          // bit 0: make the first pipeline stage never complete
@@ -31,12 +32,16 @@ struct GemmLaunch {
     GemmArgs args;
     int bn;
     bool grouped;
-    unsigned grid;
+    bool pair;               // 2-CTA clusters with the 2-CTA MMA (dense only)
+    unsigned grid;           // CTAs (a multiple of 2 in pair mode)
     cudaStream_t stream;
 };
 
 cudaError_t launch_gemm(const GemmLaunch& g);
 int gemm_stages(int bn);
+// Pair mode: how many 2-CTA clusters of the dense kernel fit on the device
+// at once (0 if none or on error).
+int gemm_pair_max_clusters(int bn);
 cudaError_t read_device_status(cudaStream_t stream, uint32_t* out, bool clear);
 
 }  // namespace fp8q

@@ -30,6 +30,8 @@ lib.fp8q_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
 lib.fp8q_set_wait_timeout_ns.restype = None
 lib.fp8q_set_gemm_tile_n.argtypes = [ctypes.c_int]
 lib.fp8q_set_gemm_tile_n.restype = ctypes.c_int
+lib.fp8q_set_gemm_pairs.argtypes = [ctypes.c_int]
+lib.fp8q_set_gemm_pairs.restype = ctypes.c_int
 lib.fp8q_status_string.argtypes = [ctypes.c_int]
 lib.fp8q_status_string.restype = ctypes.c_char_p
 for _f in ("fp8q_quant_act", "fp8q_quant_weight", "fp8_block_gemm", "fp8_grouped_gemm",
@@ -181,3 +183,8 @@ def fp8q_set_wait_timeout_ns(ns: int) -> None:
 def fp8q_set_gemm_tile_n(bn: int) -> None:
     """Force the dense GEMM's output-tile width (128 or 256; 0 = automatic)."""
     _check(lib.fp8q_set_gemm_tile_n(int(bn)), "fp8q_set_gemm_tile_n")
+
+
+def fp8q_set_gemm_pairs(enable: bool) -> None:
+    """Allow (default) or forbid 2-SM pair tiles in the dense GEMM."""
+    _check(lib.fp8q_set_gemm_pairs(int(bool(enable))), "fp8q_set_gemm_pairs")

@@ -151,6 +151,15 @@ FP8Q_API void fp8q_set_wait_timeout_ns(uint64_t ns);
  */
 FP8Q_API int fp8q_set_gemm_tile_n(int bn);
 
+/*
+ * Whether fp8_block_gemm may run a 256 x 256 output tile on a pair of SMs
+ * (2-CTA clusters with the 2-CTA tensor-core MMA, each SM holding half of
+ * the B tile). 1 (the default) uses pairs when the tile width is 256 and
+ * M > 128; 0 keeps one SM per 128 x N tile. Affects speed only, never
+ * results. Returns FP8Q_OK.
+ */
+FP8Q_API int fp8q_set_gemm_pairs(int enable);
+
 /* A short English description of a status code. Never NULL. */
 FP8Q_API const char* fp8q_status_string(int status);
 
