@@ -31,6 +31,7 @@ std::mutex g_mutex;
 uint64_t g_timeout_ns = 1000000000ull;
 int g_force_bn = 0;
 int g_pair_mode = 1;  // 1: use 2-CTA pairs for the dense GEMM where they fit
+uint32_t g_inject = 0;  // FP8Q_INJECT_* bits for failure-path tests
 constexpr int64_t kI32Max = 2147483647;
 
 int current_device(DeviceInfo** out) {
@@ -129,6 +130,11 @@ void fp8q_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns = ns ? ns : 1000000000
 int fp8q_set_gemm_tile_n(int bn) {
     if (bn != 0 && bn != 128 && bn != 256) return FP8Q_ERR_UNSUPPORTED;
     g_force_bn = bn;
+    return FP8Q_OK;
+}
+
+int fp8q_set_fault_injection(uint32_t flags) {
+    g_inject = flags & FP8Q_INJECT_STALLED_STAGE;
     return FP8Q_OK;
 }
 
@@ -237,7 +243,7 @@ int fp8_block_gemm(const void* A, const float* sa, const void* B, const float* s
     if (units > kI32Max) return FP8Q_ERR_SHAPE;
     a.num_tiles = static_cast<int32_t>(units);
     a.timeout_ns = g_timeout_ns;
-    a.debug = 0;
+    a.debug = g_inject;
     if (pair) {
         const int64_t clusters = units < dev->pair_clusters ? units : dev->pair_clusters;
         g.grid = static_cast<unsigned>(2 * clusters);
@@ -296,7 +302,7 @@ int fp8_grouped_gemm(const void* A, const float* sa, const void* B, const float*
     if ((cdiv(total_M, 128) + E) * a.nt_count > kI32Max) return FP8Q_ERR_SHAPE;
     a.num_tiles = 0;
     a.timeout_ns = g_timeout_ns;
-    a.debug = 0;
+    a.debug = g_inject;
     g.grid = static_cast<unsigned>(dev->sms);
     return fp8q::launch_gemm(g) == cudaSuccess ? FP8Q_OK : FP8Q_ERR_CUDA;
 }

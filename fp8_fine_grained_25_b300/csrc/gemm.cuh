@@ -22,7 +22,7 @@ struct GemmArgs {
     int32_t mp_count;        // pair mode: ceil(mt_count / 2) row units
     int32_t num_tiles;       // dense only; the grouped kernel counts its own
     uint64_t timeout_ns;
-    uint32_t debug;          // bit 0: make the first pipeline stage never complete
+    uint32_t debug;          // FP8Q_INJECT_STALLED_STAGE: first pipeline stage never completes
 };
 
 struct GemmLaunch {

@@ -32,6 +32,8 @@ lib.fp8q_set_gemm_tile_n.argtypes = [ctypes.c_int]
 lib.fp8q_set_gemm_tile_n.restype = ctypes.c_int
 lib.fp8q_set_gemm_pairs.argtypes = [ctypes.c_int]
 lib.fp8q_set_gemm_pairs.restype = ctypes.c_int
+lib.fp8q_set_fault_injection.argtypes = [ctypes.c_uint32]
+lib.fp8q_set_fault_injection.restype = ctypes.c_int
 lib.fp8q_status_string.argtypes = [ctypes.c_int]
 lib.fp8q_status_string.restype = ctypes.c_char_p
 for _f in ("fp8q_quant_act", "fp8q_quant_weight", "fp8_block_gemm", "fp8_grouped_gemm",
@@ -41,6 +43,7 @@ for _f in ("fp8q_quant_act", "fp8q_quant_weight", "fp8_block_gemm", "fp8_grouped
 OK, ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_DEVICE, ERR_CUDA, ERR_TIMEOUT, ERR_UNSUPPORTED, ERR_OFFSETS = range(9)
 DEVSTATUS_TIMEOUT = 0x1
 DEVSTATUS_BAD_OFFSETS = 0x2
+INJECT_STALLED_STAGE = 0x1
 
 CODE_DTYPES = (torch.uint8, torch.float8_e4m3fn)
 
@@ -188,3 +191,9 @@ def fp8q_set_gemm_tile_n(bn: int) -> None:
 def fp8q_set_gemm_pairs(enable: bool) -> None:
     """Allow (default) or forbid 2-SM pair tiles in the dense GEMM."""
     _check(lib.fp8q_set_gemm_pairs(int(bool(enable))), "fp8q_set_gemm_pairs")
+
+
+def fp8q_set_fault_injection(flags: int) -> None:
+    """Test hook: INJECT_STALLED_STAGE makes every GEMM launch time out (see
+    include/fp8q.h); 0 turns it off."""
+    _check(lib.fp8q_set_fault_injection(int(flags)), "fp8q_set_fault_injection")

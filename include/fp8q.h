@@ -160,6 +160,19 @@ FP8Q_API int fp8q_set_gemm_tile_n(int bn);
  */
 FP8Q_API int fp8q_set_gemm_pairs(int enable);
 
+/*
+ * Failure injection for tests of the device-side failure path. With
+ * FP8Q_INJECT_STALLED_STAGE set, every fp8_block_gemm / fp8_grouped_gemm
+ * launch announces 16 more bytes for its first pipeline stage than the
+ * stage receives, so that stage never completes: the kernel's bounded waits
+ * expire (see fp8q_set_wait_timeout_ns), it drains its copies, frees its
+ * tensor memory, writes nothing further, returns, and the device status word
+ * gets FP8Q_DEVSTATUS_TIMEOUT. The CUDA context stays usable. 0 (the
+ * default) turns injection off. Returns FP8Q_OK.
+ */
+#define FP8Q_INJECT_STALLED_STAGE 0x1u
+FP8Q_API int fp8q_set_fault_injection(uint32_t flags);
+
 /* A short English description of a status code. Never NULL. */
 FP8Q_API const char* fp8q_status_string(int status);
 
