@@ -70,7 +70,10 @@ struct Layout {
     static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // rows of B this CTA loads
     static constexpr int B_BYTES = B_ROWS * BK;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int EPI_WARP_BYTES = 32 * 32 * 2;  // 32 rows x 32 bf16, 64-byte swizzle
+    // two 32 rows x 32 bf16 staging boxes per warp (64-byte swizzle): one is
+    // filled while the TMA store of the other is still reading
+    static constexpr int EPI_BOX_BYTES = 32 * 32 * 2;
+    static constexpr int EPI_WARP_BYTES = 2 * EPI_BOX_BYTES;
     static constexpr int EPI_BYTES = GROUPED ? 0 : kEpiWarps * EPI_WARP_BYTES;
     // slot: sa as [128 rows][kScaleKb], then sb as [kMaxNb][kScaleKb]
     static constexpr int SCALE_SLOT_BYTES = 4 * kScaleKb * (BM + kMaxNb);
@@ -518,13 +521,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
 
             if constexpr (!GROUPED) {
-                // bf16 -> 64-byte-swizzled staging (32 rows x 64 B per warp)
-                // -> TMA store, 32 columns at a time
-                uint8_t* ebuf = smem + L::EPI_OFF + ew * L::EPI_WARP_BYTES;
-                const uint32_t ebuf_s = sbase + L::EPI_OFF + ew * L::EPI_WARP_BYTES;
+                // bf16 -> 64-byte-swizzled staging (32 rows x 64 B per box,
+                // two boxes per warp) -> TMA store, 32 columns at a time
+                uint8_t* ebuf0 = smem + L::EPI_OFF + ew * L::EPI_WARP_BYTES;
+                const uint32_t ebuf0_s = sbase + L::EPI_OFF + ew * L::EPI_WARP_BYTES;
 #pragma unroll
                 for (int c2 = 0; c2 < L::HALF / 32; ++c2) {
-                    if (lane == 0) bulk_wait_group_read0();
+                    uint8_t* ebuf = ebuf0 + (c2 & 1) * L::EPI_BOX_BYTES;
+                    const uint32_t ebuf_s = ebuf0_s + (c2 & 1) * L::EPI_BOX_BYTES;
+                    // the store issued two boxes ago (same buffer) must have read it
+                    if (lane == 0) bulk_wait_group_read1();
                     __syncwarp();
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
