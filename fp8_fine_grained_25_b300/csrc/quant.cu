@@ -264,16 +264,21 @@ __global__ void __launch_bounds__(kActThreads, 1) quant_act_kernel(const ActArgs
 
 // ---------------------------------------------------------------- weights
 // One 128x128 block per stage, loaded as one 2-D TMA box (zero fill past the
-// N and K edges). Consumer thread i owns the 16-byte chunks c = i + 512 j
-// (j = 0..3): block row c / 16, columns [8 (c % 16), +8).
+// N and K edges). The consumer warps form two groups that take alternate
+// blocks (the CTA's i-th block goes to stage i mod 4 and group i mod 2), so
+// two blocks are encoded at once. Thread i of a group owns the 16-byte
+// chunks c = i + 256 j (j = 0..7): block row c / 16, columns [8 (c % 16), +8).
 constexpr int kWConsumerWarps = 16;
-constexpr int kWChunksPerThread = 2048 / (32 * kWConsumerWarps);
+constexpr int kWGroups = 2;  // warp groups working on alternate blocks
+constexpr int kWGroupWarps = kWConsumerWarps / kWGroups;
+constexpr int kWChunksPerThread = 2048 / (32 * kWGroupWarps);
 constexpr int kWStages = 4;
 constexpr int kWStageBytes = 128 * 128 * 2;
 constexpr int kWThreads = 32 * (1 + kWConsumerWarps);
-// barriers: full[S], empty[S], red (the per-block amax exchange)
-constexpr int kWBars = 2 * kWStages + 1;
+// barriers: full[S], empty[S], red[groups] (the per-block amax exchange)
+constexpr int kWBars = 2 * kWStages + kWGroups;
 constexpr int kWSmem = kWStages * kWStageBytes + 8 * kWBars + 16 + 2 * 4 * kWConsumerWarps + 1024;
+static_assert(kWStages % kWGroups == 0, "each group must cycle through its own stages");
 
 struct WeightArgs {
     uint8_t* q;  // [N, K]
@@ -292,7 +297,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
     const uint32_t bar_base = sbase + kWStages * kWStageBytes;
     auto full = [&](int s) { return bar_base + 8u * s; };
     auto empty = [&](int s) { return bar_base + 8u * (kWStages + s); };
-    const uint32_t red_bar = bar_base + 8u * (2 * kWStages);
+    auto red_bar = [&](int g) { return bar_base + 8u * (2 * kWStages + g); };
     uint8_t* misc = smem_raw + pad + kWStages * kWStageBytes + 8 * kWBars;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc);
     float* red = reinterpret_cast<float*>(misc + 16);  // [2][kWConsumerWarps]
@@ -302,9 +307,9 @@ __global__ void __launch_bounds__(kWThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < kWStages; ++s) {
             mbar_init(full(s), 1);
-            mbar_init(empty(s), kWConsumerWarps);
+            mbar_init(empty(s), kWGroupWarps);
         }
-        mbar_init(red_bar, kWConsumerWarps);
+        for (int g = 0; g < kWGroups; ++g) mbar_init(red_bar(g), kWGroupWarps);
         *abort_flag = 0;
         fence_barrier_init();
         fence_proxy_async_smem();
@@ -338,15 +343,18 @@ __global__ void __launch_bounds__(kWThreads, 1)
         }
     } else {
         const int cw = warp - 1;
-        const uint32_t tid = threadIdx.x - 32;
-        int stage = 0;
+        const int grp = cw / kWGroupWarps, gw = cw % kWGroupWarps;
+        const uint32_t tid = static_cast<uint32_t>(gw * 32 + lane);  // thread within the group
+        float* red_g = red + grp * 2 * kWGroupWarps;                  // [2][kWGroupWarps]
+        int stage = grp;
         uint32_t phase = 0, iter = 0;
-        for (uint64_t b = blockIdx.x; b < nblocks; b += gridDim.x, ++iter) {
+        for (uint64_t b = blockIdx.x + static_cast<uint64_t>(grp) * gridDim.x; b < nblocks;
+             b += static_cast<uint64_t>(kWGroups) * gridDim.x, ++iter) {
             if (!warp_wait(full(stage), phase, abort_flag, a.timeout_ns)) break;
             const uint32_t nb = static_cast<uint32_t>(b / a.KB);
             const uint32_t kb = static_cast<uint32_t>(b - static_cast<uint64_t>(nb) * a.KB);
             const uint32_t st = sbase + stage * kWStageBytes;
-            constexpr uint32_t kStride = 32 * kWConsumerWarps;
+            constexpr uint32_t kStride = 32 * kWGroupWarps;
             uint4 v[kWChunksPerThread];
 #pragma unroll
             for (int j = 0; j < kWChunksPerThread; ++j) v[j] = lds16(st + 16u * (tid + kStride * j));
@@ -357,19 +365,20 @@ __global__ void __launch_bounds__(kWThreads, 1)
             for (int j = 0; j < kWChunksPerThread; ++j) bits = max(bits, absmax_bits8(v[j]));
 #pragma unroll
             for (int d = 16; d >= 1; d >>= 1) bits = max(bits, __shfl_xor_sync(0xFFFFFFFFu, bits, d));
-            // Block amax across the consumer warps: each publishes its partial
-            // in one half of red[] (alternating per block, so a warp that is a
-            // block ahead never overwrites values still being read) and arrives
-            // on red_bar; the phase of block `iter` has parity iter & 1.
-            float* rb = red + (iter & 1u) * kWConsumerWarps;
+            // Block amax across the group's warps: each publishes its partial
+            // in one half of its group's red[] (alternating per block, so a warp
+            // that is a block ahead never overwrites values still being read)
+            // and arrives on the group's barrier, whose phase for the group's
+            // block `iter` has parity iter & 1.
+            float* rb = red_g + (iter & 1u) * kWGroupWarps;
             if (lane == 0) {
-                rb[cw] = __uint_as_float(bits << 16);
-                mbar_arrive(red_bar);
+                rb[gw] = __uint_as_float(bits << 16);
+                mbar_arrive(red_bar(grp));
             }
-            if (!warp_wait(red_bar, iter & 1u, abort_flag, a.timeout_ns)) break;
+            if (!warp_wait(red_bar(grp), iter & 1u, abort_flag, a.timeout_ns)) break;
             float amax = rb[0];
 #pragma unroll
-            for (int i = 1; i < kWConsumerWarps; ++i) amax = fmaxf(amax, rb[i]);
+            for (int i = 1; i < kWGroupWarps; ++i) amax = fmaxf(amax, rb[i]);
             const float sc = tile_scale(amax);
             const bool fast = amax >= kFastDivMinAmax;
             const float r = fast ? __frcp_rn(sc) : 0.0f;
@@ -382,8 +391,9 @@ __global__ void __launch_bounds__(kWThreads, 1)
                     *reinterpret_cast<uint2*>(a.q + n * a.K + k) = encode8_r(v[j], sc, r, fast);
             }
             if (tid == 0) a.s[b] = sc;
-            if (++stage == kWStages) {
-                stage = 0;
+            stage += kWGroups;
+            if (stage >= kWStages) {
+                stage -= kWStages;
                 phase ^= 1u;
             }
         }
