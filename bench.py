@@ -8,7 +8,8 @@ activations per 1x128 tile, quantize the bf16 weights per 128x128 block
 and run the block-scaled FP8 GEMM with FP32 promotion. The default workload
 is the dense 7168-square layer (A [8192, 7168] with outlier channels,
 B [7168, 7168]); --config 4 times the grouped MoE GEMM path instead
-(32768 routed rows, 256 experts of [2048, 7168]).
+(32768 routed rows, 256 experts of [2048, 7168]); --config 2 / 6 time the MLA
+down-projections as two GEMMs / as one GEMM on the stacked Wq||Wkv.
 
 The printed JSON line reports whole-step TFLOP/s (2*M*N*K per step over the
 step time), the per-kernel times (CUDA events on the launching stream), the
@@ -280,7 +281,7 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5, 6])
     ap.add_argument("--e2e-steps", type=int, default=10)
     args = ap.parse_args()
     if args.warmup < 3:

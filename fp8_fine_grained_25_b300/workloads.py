@@ -95,6 +95,17 @@ def mla_down(seed: int = 0, device="cpu", tokens: int = 4096) -> Workload:
                                         seed * 1000 + 3, device)})
 
 
+def mla_down_fused(seed: int = 0, device="cpu", tokens: int = 4096) -> Workload:
+    """The MLA down-projections as one GEMM: the same A and the same Wq, Wkv
+    draws as mla_down, with the weights stacked row-wise into Wq‖Wkv
+    [2112, 7168]. 1536 is a multiple of 128, so the 128x128 weight blocks and
+    their scales are those of the two separate weights, and the output's
+    columns [0, 1536) and [1536, 2112) are the two projections."""
+    w = mla_down(seed, device, tokens)
+    Wqkv = torch.cat([w.weights["Wq"], w.weights["Wkv"]], dim=0)
+    return Workload(f"MLA down-proj fused {tokens}x2112x7168 (Wq||Wkv)", w.A, {"Wqkv": Wqkv})
+
+
 def dense_square(seed: int = 0, device="cpu", M: int = 8192) -> Workload:
     """A [M, 7168] ~ N(0,1) with 0.1% outlier channels x100; B [7168, 7168]
     ~ N(0, 0.01^2)."""
@@ -124,4 +135,4 @@ def large_m(seed: int = 0, device="cpu", M: int = 32768) -> Workload:
                     {"B": normal_bf16((18432, HIDDEN), 0.01, seed * 1000 + 2, device)})
 
 
-CONFIGS = {1: tiny, 2: mla_down, 3: dense_square, 4: moe_grouped, 5: large_m}
+CONFIGS = {1: tiny, 2: mla_down, 3: dense_square, 4: moe_grouped, 5: large_m, 6: mla_down_fused}

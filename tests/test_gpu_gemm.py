@@ -162,3 +162,24 @@ def test_gemm_large_m_full_size(q):
     from fp8_fine_grained_25_b300 import workloads
     w = workloads.large_m(seed=0, device=DEV)
     _sampled_check(q, w.A, w.weights["B"], "large-M 32768x18432x7168", n_rows=96, n_cols=32)
+
+
+@pytest.mark.slow
+def test_mla_fused_equals_separate_projections(q):
+    """Stacking Wq||Wkv (1536 = 12 * 128, so the 128x128 blocks line up) gives
+    one GEMM whose column ranges are the two projections, bit for bit; the
+    fused output is also checked against the oracle on sampled rows."""
+    from fp8_fine_grained_25_b300 import workloads
+    sep = workloads.mla_down(seed=0, device=DEV)
+    fused = workloads.mla_down_fused(seed=0, device=DEV)
+    qa, sa = q.fp8q_quant_act(sep.A)
+    outs = []
+    for name in ("Wq", "Wkv"):
+        qb, sb = q.fp8q_quant_weight(sep.weights[name])
+        outs.append(q.fp8_block_gemm(qa, sa, qb, sb))
+    qf, sf = q.fp8q_quant_weight(fused.weights["Wqkv"])
+    Cf = q.fp8_block_gemm(qa, sa, qf, sf)
+    torch.cuda.synchronize()
+    assert torch.equal(Cf[:, :1536].view(torch.int16), outs[0].view(torch.int16))
+    assert torch.equal(Cf[:, 1536:].view(torch.int16), outs[1].view(torch.int16))
+    _sampled_check(q, fused.A, fused.weights["Wqkv"], "MLA fused Wq||Wkv", n_rows=64, n_cols=32)
