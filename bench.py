@@ -9,7 +9,8 @@ and run the block-scaled FP8 GEMM with FP32 promotion. The default workload
 is the dense 7168-square layer (A [8192, 7168] with outlier channels,
 B [7168, 7168]); --config 4 times the grouped MoE GEMM path instead
 (32768 routed rows, 256 experts of [2048, 7168]); --config 2 / 6 time the MLA
-down-projections as two GEMMs / as one GEMM on the stacked Wq||Wkv.
+down-projections as two GEMMs / as one GEMM on the stacked Wq||Wkv; --config 7
+runs the MoE step as quantize-the-tokens-then-dispatch-in-FP8.
 
 The printed JSON line reports whole-step TFLOP/s (2*M*N*K per step over the
 step time), the per-kernel times (CUDA events on the launching stream), the
@@ -162,6 +163,10 @@ def step_flops(w) -> float:
     return 2.0 * M * N * K
 
 
+def args_dispatch(w) -> bool:
+    return w.index is not None and "dispatch" in w.name
+
+
 class Path:
     """The hot path on one device: buffers allocated once, one call per step."""
 
@@ -186,16 +191,29 @@ class Path:
                 C = torch.empty((M, W.shape[0]), dtype=torch.bfloat16, device=device)
             self.bufs[name] = (qb, sb, C)
         self.launches_per_step = 1 + 2 * len(w.weights)
+        # FP8 dispatch: quantize the T tokens, then gather rows into expert order
+        self.dispatch = args_dispatch(w)
+        if self.dispatch:
+            T = w.tokens.shape[0]
+            self.qx = torch.empty((T, K), dtype=torch.uint8, device=device)
+            self.sx = torch.empty((T, -(-K // 128)), dtype=torch.float32, device=device)
+            self.launches_per_step += 1
 
     def step(self, A=None, weights=None, events=None, outs=None, stream=None):
         """One pass of the path; `outs` optionally maps weight name -> C
         buffer, `stream` the CUDA stream (default: the current one)."""
         f = self.fp8q
-        A = self.w.A if A is None else A
+        if not self.dispatch:
+            A = self.w.A if A is None else A
         weights = self.w.weights if weights is None else weights
         rec = (lambda i: events[i].record(stream)) if events is not None else (lambda i: None)
         rec(0)
-        f.fp8q_quant_act(A, self.qa, self.sa, stream=stream)
+        if self.dispatch:
+            X = self.w.tokens if A is None else A
+            f.fp8q_quant_act(X, self.qx, self.sx, stream=stream)
+            f.fp8q_gather_rows(self.qx, self.sx, self.w.index, self.qa, self.sa, stream=stream)
+        else:
+            f.fp8q_quant_act(A, self.qa, self.sa, stream=stream)
         rec(1)
         i = 2
         for name, W in weights.items():
@@ -281,7 +299,7 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5, 6])
+    ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5, 6, 7])
     ap.add_argument("--e2e-steps", type=int, default=10)
     args = ap.parse_args()
     if args.warmup < 3:
@@ -339,8 +357,13 @@ def main():
 
     M, K = w.A.shape
     kern = {}
-    kern["quant_act"] = {"ms": per["quant_act"] * 1e3,
-                         "GB/s": (3 * M * K + 4 * M * -(-K // 128)) / per["quant_act"] / 1e9}
+    if path.dispatch:
+        T = w.tokens.shape[0]
+        qbytes = 3 * T * K + 4 * T * -(-K // 128) + 2 * (M * K + 4 * M * -(-K // 128))
+        kern["quant_act+dispatch"] = {"ms": per["quant_act"] * 1e3, "GB/s": qbytes / per["quant_act"] / 1e9}
+    else:
+        kern["quant_act"] = {"ms": per["quant_act"] * 1e3,
+                             "GB/s": (3 * M * K + 4 * M * -(-K // 128)) / per["quant_act"] / 1e9}
     for n, W in w.weights.items():
         e = W.numel()
         blocks = e // W.shape[-1] // 128 * -(-W.shape[-1] // 128)
@@ -393,11 +416,11 @@ def main():
     # duplex); events order each buffer's reuse.
     e2e = None
     if args.e2e_steps > 0:
-        hostA = w.A.cpu().pin_memory()
+        hostA = (w.tokens if path.dispatch else w.A).cpu().pin_memory()
         hostW = {n: W.cpu().pin_memory() for n, W in w.weights.items()}
         hostC = {n: torch.empty(path.bufs[n][2].shape, dtype=torch.bfloat16).pin_memory()
                  for n in w.weights}
-        devA = [torch.empty_like(w.A) for _ in range(2)]
+        devA = [torch.empty_like(w.tokens if path.dispatch else w.A) for _ in range(2)]
         devW = [{n: torch.empty_like(W) for n, W in w.weights.items()} for _ in range(2)]
         devC = [{n: torch.empty_like(path.bufs[n][2]) for n in w.weights} for _ in range(2)]
         s_in, s_cmp, s_out = (torch.cuda.Stream(device) for _ in range(3))

@@ -188,6 +188,24 @@ int fp8q_quant_weight(const void* w_bf16, int64_t N, int64_t K, void* q_e4m3, fl
                : FP8Q_ERR_CUDA;
 }
 
+int fp8q_gather_rows(const void* q_src, const float* s_src, int64_t T, int64_t K,
+                     const int32_t* index, int64_t R, void* q_dst, float* s_dst,
+                     cudaStream_t stream) {
+    if (T < 0 || R < 0 || K <= 0 || T > kI32Max || R > kI32Max || K > kI32Max)
+        return FP8Q_ERR_SHAPE;
+    if (R == 0) return FP8Q_OK;
+    if (!q_src || !s_src || !index || !q_dst || !s_dst) return FP8Q_ERR_NULL;
+    if (K % 16 != 0 || !aligned(q_src, 16) || !aligned(q_dst, 16) || !aligned(s_src, 4) ||
+        !aligned(s_dst, 4) || !aligned(index, 4))
+        return FP8Q_ERR_ALIGN;
+    DeviceInfo* dev = nullptr;
+    if (int rc = current_device(&dev)) return rc;
+    return fp8q::launch_gather_rows(q_src, s_src, T, K, index, R, q_dst, s_dst, stream, dev->sms) ==
+                   cudaSuccess
+               ? FP8Q_OK
+               : FP8Q_ERR_CUDA;
+}
+
 int fp8_block_gemm(const void* A, const float* sa, const void* B, const float* sb, void* C_bf16,
                    int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
     if (M < 0 || N <= 0 || K <= 0 || M > kI32Max || N > kI32Max || K > kI32Max)

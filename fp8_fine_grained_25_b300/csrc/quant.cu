@@ -402,7 +402,57 @@ __global__ void __launch_bounds__(kWThreads, 1)
     if (threadIdx.x == 0 && *abort_flag) atomicOr(&g_quant_status, FP8Q_DEVSTATUS_TIMEOUT);
 }
 
+// ------------------------------------------------------------------ gather
+// One warp per output row: the row's K code bytes move as 16-byte vectors
+// (four in flight per lane), its ceil(K/128) scales as 4-byte words.
+constexpr int kGatherThreads = 256;
+
+__global__ void __launch_bounds__(kGatherThreads) gather_rows_kernel(
+    const uint8_t* __restrict__ q_src, const float* __restrict__ s_src, int64_t T, int64_t K,
+    uint32_t KB, const int32_t* __restrict__ index, int64_t R, uint8_t* __restrict__ q_dst,
+    float* __restrict__ s_dst) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const int64_t vecs = K / 16;
+    for (int64_t r = warp; r < R; r += nwarps) {
+        const int64_t src = __ldg(index + r);
+        const bool ok = src >= 0 && src < T;
+        if (!ok && lane == 0) atomicOr(&g_quant_status, FP8Q_DEVSTATUS_BAD_INDEX);
+        const uint4* in = reinterpret_cast<const uint4*>(q_src + (ok ? src : 0) * K);
+        uint4* out = reinterpret_cast<uint4*>(q_dst + r * K);
+        for (int64_t v0 = 0; v0 < vecs; v0 += 4 * 32) {
+            uint4 buf[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int64_t v = v0 + u * 32 + lane;
+                buf[u] = (ok && v < vecs) ? __ldg(in + v) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int64_t v = v0 + u * 32 + lane;
+                if (v < vecs) out[v] = buf[u];
+            }
+        }
+        for (uint32_t j = lane; j < KB; j += 32)
+            s_dst[r * KB + j] = ok ? __ldg(s_src + src * KB + j) : 0.0f;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_gather_rows(const void* q_src, const float* s_src, int64_t T, int64_t K,
+                               const int32_t* index, int64_t R, void* q_dst, float* s_dst,
+                               cudaStream_t stream, int num_sms) {
+    const int64_t warps_wanted = R;
+    const int64_t blocks_wanted = (warps_wanted + kGatherThreads / 32 - 1) / (kGatherThreads / 32);
+    const int64_t cap = static_cast<int64_t>(num_sms) * (2048 / kGatherThreads);
+    const unsigned grid = static_cast<unsigned>(blocks_wanted < cap ? blocks_wanted : cap);
+    gather_rows_kernel<<<grid, kGatherThreads, 0, stream>>>(
+        static_cast<const uint8_t*>(q_src), s_src, T, K, static_cast<uint32_t>((K + 127) / 128),
+        index, R, static_cast<uint8_t*>(q_dst), s_dst);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_quant_act(const void* x, int64_t M, int64_t K, void* q, float* s,
                              cudaStream_t stream, int num_sms, uint64_t timeout_ns) {

@@ -12,6 +12,9 @@ cudaError_t launch_quant_act(const void* x, int64_t M, int64_t K, void* q, float
 // tmW: bf16 [N, K] tensor map, box 128 x 128, no swizzle
 cudaError_t launch_quant_weight(const CUtensorMap* tmW, void* q, float* s, int64_t N, int64_t K,
                                 cudaStream_t stream, int num_sms, uint64_t timeout_ns);
+cudaError_t launch_gather_rows(const void* q_src, const float* s_src, int64_t T, int64_t K,
+                               const int32_t* index, int64_t R, void* q_dst, float* s_dst,
+                               cudaStream_t stream, int num_sms);
 cudaError_t read_quant_status(uint32_t* out, bool clear);
 
 }  // namespace fp8q

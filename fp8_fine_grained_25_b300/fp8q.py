@@ -24,6 +24,8 @@ _i64, _i32, _p = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p
 lib.fp8q_quant_act.argtypes = [_p, _i64, _i64, _p, _p, _p]
 lib.fp8q_quant_weight.argtypes = [_p, _i64, _i64, _p, _p, _p]
 lib.fp8_block_gemm.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p]
+lib.fp8q_gather_rows.argtypes = [_p, _p, _i64, _i64, _p, _i64, _p, _p, _p]
+lib.fp8q_gather_rows.restype = ctypes.c_int
 lib.fp8_grouped_gemm.argtypes = [_p, _p, _p, _p, _p, _p, _i32, _i64, _i64, _i64, _p]
 lib.fp8q_get_device_status.argtypes = [_p, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
 lib.fp8q_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
@@ -43,6 +45,7 @@ for _f in ("fp8q_quant_act", "fp8q_quant_weight", "fp8_block_gemm", "fp8_grouped
 OK, ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_DEVICE, ERR_CUDA, ERR_TIMEOUT, ERR_UNSUPPORTED, ERR_OFFSETS = range(9)
 DEVSTATUS_TIMEOUT = 0x1
 DEVSTATUS_BAD_OFFSETS = 0x2
+DEVSTATUS_BAD_INDEX = 0x4
 INJECT_STALLED_STAGE = 0x1
 
 CODE_DTYPES = (torch.uint8, torch.float8_e4m3fn)
@@ -126,6 +129,29 @@ def fp8q_quant_weight(w: torch.Tensor, q: torch.Tensor | None = None,
     _check(lib.fp8q_quant_weight(w.data_ptr(), rows, K, q.data_ptr(), scales.data_ptr(),
                                  _stream(stream)), "fp8q_quant_weight")
     return q, scales
+
+
+def fp8q_gather_rows(q_src: torch.Tensor, s_src: torch.Tensor, index: torch.Tensor,
+                     q_dst: torch.Tensor | None = None, s_dst: torch.Tensor | None = None,
+                     stream=None):
+    """Rows index[r] of quantized activations (codes [T, K], scales [T, KB])
+    -> (codes [R, K], scales [R, KB]): the MoE dispatch in FP8."""
+    T, K = q_src.shape
+    R = index.shape[0]
+    KB = _cdiv(K, 128)
+    _need(q_src, "q_src", CODE_DTYPES, (T, K))
+    _need(s_src, "s_src", (torch.float32,), (T, KB))
+    _need(index, "index", (torch.int32,), (R,))
+    if q_dst is None:
+        q_dst = torch.empty((R, K), dtype=q_src.dtype, device=q_src.device)
+    if s_dst is None:
+        s_dst = torch.empty((R, KB), dtype=torch.float32, device=q_src.device)
+    _need(q_dst, "q_dst", CODE_DTYPES, (R, K))
+    _need(s_dst, "s_dst", (torch.float32,), (R, KB))
+    _check(lib.fp8q_gather_rows(q_src.data_ptr(), s_src.data_ptr(), T, K, index.data_ptr(), R,
+                                q_dst.data_ptr(), s_dst.data_ptr(), _stream(stream)),
+           "fp8q_gather_rows")
+    return q_dst, s_dst
 
 
 def fp8_block_gemm(A: torch.Tensor, sa: torch.Tensor, B: torch.Tensor, sb: torch.Tensor,

@@ -76,6 +76,8 @@ class Workload:
     weights: dict = field(default_factory=dict)  # name -> bf16 [N, K] or [E, N, K]
     offsets: torch.Tensor | None = None   # int32 [E+1] for the grouped GEMM
     note: str = ""
+    tokens: torch.Tensor | None = None    # MoE: the un-gathered token activations [T, K]
+    index: torch.Tensor | None = None     # MoE: int32 token of each routed row (A = tokens[index])
 
 
 def tiny(seed: int = 0, device="cpu") -> Workload:
@@ -125,7 +127,18 @@ def moe_grouped(seed: int = 0, device="cpu", T: int = 4096, E: int = N_ROUTED,
     for e in range(E):  # per expert, to bound the fp32 scratch
         W[e] = normal_bf16((N, K), 0.01, seed * 1000 + 10 + e, device)
     return Workload(f"MoE grouped T={T} E={E} top{top_k} {N}x{K}", X[token], {"W": W},
-                    offsets, note="rows gathered in expert order")
+                    offsets, note="rows gathered in expert order", tokens=X,
+                    index=token.to(torch.int32))
+
+
+def moe_dispatch_fp8(seed: int = 0, device="cpu", **kw) -> Workload:
+    """The MoE workload run as quantize-then-dispatch: the step quantizes the
+    T tokens once and gathers codes and scales into expert order (the same
+    data as moe_grouped)."""
+    w = moe_grouped(seed, device, **kw)
+    w.name = w.name.replace("MoE grouped", "MoE FP8 dispatch")
+    w.note = "tokens quantized once, FP8 rows gathered in expert order"
+    return w
 
 
 def large_m(seed: int = 0, device="cpu", M: int = 32768) -> Workload:
@@ -135,4 +148,5 @@ def large_m(seed: int = 0, device="cpu", M: int = 32768) -> Workload:
                     {"B": normal_bf16((18432, HIDDEN), 0.01, seed * 1000 + 2, device)})
 
 
-CONFIGS = {1: tiny, 2: mla_down, 3: dense_square, 4: moe_grouped, 5: large_m, 6: mla_down_fused}
+CONFIGS = {1: tiny, 2: mla_down, 3: dense_square, 4: moe_grouped, 5: large_m, 6: mla_down_fused,
+           7: moe_dispatch_fp8}

@@ -70,6 +70,7 @@ typedef enum {
 /* Device status word bits (see fp8q_get_device_status). */
 #define FP8Q_DEVSTATUS_TIMEOUT 0x1u
 #define FP8Q_DEVSTATUS_BAD_OFFSETS 0x2u
+#define FP8Q_DEVSTATUS_BAD_INDEX 0x4u
 
 /*
  * Activation quantization, one scale per 1x128 tile (Fig. 7a, "1x128
@@ -95,6 +96,25 @@ FP8Q_API int fp8q_quant_act(const void* x_bf16, int64_t M, int64_t K, void* q_e4
  */
 FP8Q_API int fp8q_quant_weight(const void* w_bf16, int64_t N, int64_t K, void* q_e4m3, float* scales,
                       cudaStream_t stream);
+
+/*
+ * Row gather of quantized activations: the MoE dispatch in FP8 (news.qq.com
+ * page, "FP8 低精度训练", item "低精度存储和通信", Fig. 10: activations are
+ * stored and communicated in FP8). Quantizing the T tokens once and then
+ * moving codes and scales into expert order gives exactly the codes and
+ * scales of quantizing the gathered bf16 rows, because the 1x128 tiles are
+ * row-local.
+ *   q_src  in : E4M3 codes [T, K]        s_src in : fp32 [T, ceil(K/128)]
+ *   index  in : DEVICE int32 [R]; output row r is source row index[r]
+ *               (repeats allowed)
+ *   q_dst  out: E4M3 codes [R, K]        s_dst out: fp32 [R, ceil(K/128)]
+ * K % 16 == 0; q pointers 16-byte aligned, s and index 4-byte aligned.
+ * An index outside [0, T) gives a zero row and sets
+ * FP8Q_DEVSTATUS_BAD_INDEX in the device status word. R = 0 is a no-op.
+ */
+FP8Q_API int fp8q_gather_rows(const void* q_src, const float* s_src, int64_t T, int64_t K,
+                              const int32_t* index, int64_t R, void* q_dst, float* s_dst,
+                              cudaStream_t stream);
 
 /*
  * Block-scaled FP8 GEMM, C = A * B^T (Fig. 7b: FP8 MMA per 128-wide K block,

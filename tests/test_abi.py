@@ -119,3 +119,20 @@ def test_grouped_argument_checks(lib):
     assert _gg(lib, P, P, P, P, P, None, 4, 64, 256, 512, None) == NULL
     assert _gg(lib, P, P, P, P, P, P + 2, 4, 64, 256, 512, None) == ALIGN
     assert _gg(lib, P, P, P, P, P, P, 4, 64, 256, 500, None) == ALIGN
+
+
+def _ga(lib, *a):
+    f = lib.fp8q_gather_rows
+    f.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+                  ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    return f(*a)
+
+
+def test_gather_argument_checks(lib):
+    assert _ga(lib, P, P, -1, 128, P, 4, P, P, None) == SHAPE
+    assert _ga(lib, P, P, 8, 0, P, 4, P, P, None) == SHAPE
+    assert _ga(lib, None, None, 8, 128, None, 0, None, None, None) == OK   # R = 0
+    assert _ga(lib, P, P, 8, 128, None, 4, P, P, None) == NULL
+    assert _ga(lib, P, P, 8, 120, P, 4, P, P, None) == ALIGN
+    assert _ga(lib, P + 8, P, 8, 128, P, 4, P, P, None) == ALIGN
+    assert _ga(lib, P, P, 8, 128, P + 2, 4, P, P, None) == ALIGN
