@@ -66,6 +66,7 @@ def _load():
         lib.fp8o_quant_weight.argtypes = [p, i64, i64, i64, i64, p, p]
         lib.fp8o_block_partials.argtypes = [p, p, i64, i64, i64, p]
         lib.fp8o_gemm.argtypes = [p, p, p, p, i64, p, i64, p, i64, p, p]
+        lib.fp8o_wgrad_gemm.argtypes = [p, p, p, p, i64, p, i64, p, i64, p, p]
         lib.fp8o_grouped_gemm.argtypes = [p, p, p, p, p, ctypes.c_int32, i64, i64,
                                           p, i64, p, i64, p, p]
         _lib = lib
@@ -149,6 +150,25 @@ def quant_weight(w_bits, threads: int | None = None):
     return q, s
 
 
+def quant_act_t(x_bits, threads: int | None = None):
+    """Quantization of bf16 activations [M, K] in 128x1 tiles (128 consecutive
+    rows of one column), written transposed: the 1x128 tiles of x^T.
+
+    This is the layout the weight-gradient GEMM reads (it contracts over the
+    M axis). Returns (codes uint8 [K, M], scales float32 [K, ceil(M/128)])."""
+    x = _as_bf16_bits(x_bits)
+    return quant_act(np.ascontiguousarray(x.T), threads)
+
+
+def quant_weight_t(w_bits, threads: int | None = None):
+    """128x128-block quantization of bf16 weights [N, K] with the codes also
+    in the transposed layout. A block's amax, scale and codes do not depend
+    on the orientation, so the transposed outputs are the transposes:
+    returns (q [N, K], s [NB, KB], qt [K, N], st [KB, NB])."""
+    q, s = quant_weight(w_bits, threads)
+    return q, s, np.ascontiguousarray(q.T), np.ascontiguousarray(s.T)
+
+
 # --------------------------------------------------------------------- GEMM
 def block_partials(qa, qb, m: int, n: int) -> np.ndarray:
     """Exact per-128-K-block dot products of decoded codes, float64 [KB]."""
@@ -161,12 +181,7 @@ def block_partials(qa, qb, m: int, n: int) -> np.ndarray:
     return P
 
 
-def gemm(qa, sa, qb, sb, rows=None, cols=None, threads: int | None = None):
-    """Block-scaled GEMM C = A * B^T at the outputs rows x cols.
-
-    qa uint8 [M, K], sa float32 [M, KB], qb uint8 [N, K], sb float32 [NB, KB].
-    Returns (c32 float32 [len(rows), len(cols)], S float64 [same])."""
-    lib = _load()
+def _gemm_at(fn, qa, sa, qb, sb, rows, cols, threads):
     qa = np.ascontiguousarray(qa, dtype=np.uint8)
     qb = np.ascontiguousarray(qb, dtype=np.uint8)
     sa = np.ascontiguousarray(sa, dtype=np.float32)
@@ -184,14 +199,30 @@ def gemm(qa, sa, qb, sb, rows=None, cols=None, threads: int | None = None):
         r = rows[c[0]:c[1]]
         o = np.empty((len(r), len(cols)), dtype=np.float32)
         b = np.empty((len(r), len(cols)), dtype=np.float64)
-        lib.fp8o_gemm(_ptr(qa), _ptr(sa), _ptr(qb), _ptr(sb), K, _ptr(r), len(r),
-                      _ptr(cols), len(cols), _ptr(o), _ptr(b))
+        fn(_ptr(qa), _ptr(sa), _ptr(qb), _ptr(sb), K, _ptr(r), len(r),
+           _ptr(cols), len(cols), _ptr(o), _ptr(b))
         c32[c[0]:c[1]] = o
         S[c[0]:c[1]] = b
 
     with ThreadPoolExecutor(len(chunks)) as ex:
         list(ex.map(work, chunks))
     return c32, S
+
+
+def gemm(qa, sa, qb, sb, rows=None, cols=None, threads: int | None = None):
+    """Block-scaled GEMM C = A * B^T at the outputs rows x cols.
+
+    qa uint8 [M, K], sa float32 [M, KB], qb uint8 [N, K], sb float32 [NB, KB].
+    Returns (c32 float32 [len(rows), len(cols)], S float64 [same])."""
+    return _gemm_at(_load().fp8o_gemm, qa, sa, qb, sb, rows, cols, threads)
+
+
+def wgrad_gemm(qa, sa, qb, sb, rows=None, cols=None, threads: int | None = None):
+    """The weight-gradient GEMM: C = A * B^T where both operands carry one
+    scale per row per 128-wide K block (1x128 tiles of the transposed
+    activations): qa uint8 [M, K], sa float32 [M, KB], qb uint8 [N, K],
+    sb float32 [N, KB]. Returns (c32, S) at rows x cols."""
+    return _gemm_at(_load().fp8o_wgrad_gemm, qa, sa, qb, sb, rows, cols, threads)
 
 
 def grouped_gemm(qa, sa, qb, sb, offsets, rows, cols=None, threads: int | None = None):

@@ -206,11 +206,13 @@ void fp8o_block_partials(const uint8_t* qa, const uint8_t* qb, int64_t K, int64_
  *     acc = fl32(acc + fl32(fl32(P) * sab))
  * Also returns S = sum_k |dec(qa) * sa * dec(qb) * sb| in FP64, the scale of
  * the acceptance bound.
- *   qa [M, K], sa [M, KB]; qb [N, K], sb [ceil(N/128), KB]; row-major.
+ *   qa [M, K], sa [M, KB]; qb [N, K], sb [ceil(N/g), KB]; row-major, where
+ *   g is the number of B rows sharing one scale row: 128 for a weight
+ *   quantized in 128x128 blocks, 1 for an operand quantized in 1x128 tiles.
  */
 static void gemm_element(const double* dec, const uint8_t* qa, const float* sa,
-                         const uint8_t* qb, const float* sb, int64_t K, int64_t m, int64_t n,
-                         float* c32, double* S) {
+                         const uint8_t* qb, const float* sb, int64_t g, int64_t K, int64_t m,
+                         int64_t n, float* c32, double* S) {
     int64_t KB = (K + TILE - 1) / TILE;
     float acc = 0.0f;
     double bound = 0.0;
@@ -224,7 +226,7 @@ static void gemm_element(const double* dec, const uint8_t* qa, const float* sa,
             Pabs += fabs(prod);
         }
         float a_s = sa[m * KB + kb];
-        float b_s = sb[(n / TILE) * KB + kb];
+        float b_s = sb[(n / g) * KB + kb];
         float sab = a_s * b_s;
         float t = (float)P * sab;
         acc = acc + t;
@@ -250,7 +252,33 @@ void fp8o_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb, const floa
     decode_table(dec);
     for (int64_t i = 0; i < nrows; ++i)
         for (int64_t j = 0; j < ncols; ++j)
-            gemm_element(dec, qa, sa, qb, sb, K, rows[i], cols[j], &c32[i * ncols + j],
+            gemm_element(dec, qa, sa, qb, sb, TILE, K, rows[i], cols[j], &c32[i * ncols + j],
+                         &S[i * ncols + j]);
+}
+
+/*
+ * The weight-gradient GEMM of the backward pass, at selected outputs. The
+ * news.qq.com page's pipeline figure ("DualPipe" overlap, "backward for
+ * weights") and its FP8 section (Fig. 7: the linear layers' GEMMs run in
+ * FP8) put this contraction in FP8 too; the pages do not spell out its
+ * quantization. Reading taken: dW = dY^T X contracts over tokens, so both
+ * operands are activations quantized in 1x128 tiles along the token axis
+ * (128x1 tiles of dY [T, N] and X [T, K]), stored transposed:
+ *   qa = codes of dY^T [N, T], sa [N, ceil(T/128)]
+ *   qb = codes of X^T  [K, T], sb [K, ceil(T/128)]
+ * and the result is dW [N, K] = A * B^T, promoted per 128-token block
+ * exactly as the forward GEMM, with one B scale per row instead of per
+ * 128-row block. Here M, N and K are the rows of A, the rows of B and the
+ * contraction length.
+ */
+void fp8o_wgrad_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb,
+                     int64_t K, const int64_t* rows, int64_t nrows, const int64_t* cols,
+                     int64_t ncols, float* c32, double* S) {
+    double dec[256];
+    decode_table(dec);
+    for (int64_t i = 0; i < nrows; ++i)
+        for (int64_t j = 0; j < ncols; ++j)
+            gemm_element(dec, qa, sa, qb, sb, 1, K, rows[i], cols[j], &c32[i * ncols + j],
                          &S[i * ncols + j]);
 }
 
@@ -281,8 +309,8 @@ void fp8o_grouped_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb,
                 S[i * ncols + j] = NAN;
                 continue;
             }
-            gemm_element(dec, qa, sa, qb + (int64_t)e * N * K, sb + (int64_t)e * NB * KB, K,
-                         m, cols[j], &c32[i * ncols + j], &S[i * ncols + j]);
+            gemm_element(dec, qa, sa, qb + (int64_t)e * N * K, sb + (int64_t)e * NB * KB, TILE,
+                         K, m, cols[j], &c32[i * ncols + j], &S[i * ncols + j]);
         }
     }
 }

@@ -142,3 +142,57 @@ def test_acceptance_helpers():
     assert not ok
     ok, _, _ = oracle.gemm_check(np.array([1.01]), np.array([1.0]), np.array([1e3]))
     assert ok
+
+
+# ---- the weight-gradient GEMM: one B scale per row (1x128 tiles on both sides)
+def _exact_rows(qa, sa, qb, sb, m, n):
+    """Exact sum_k A[m,k] sa[m,k/128] B[n,k] sb[n,k/128] and sum |terms|."""
+    K = qa.shape[1]
+    total, S = Fraction(0), Fraction(0)
+    for kb in range(-(-K // 128)):
+        p, pabs = Fraction(0), Fraction(0)
+        for k in range(kb * 128, min(K, kb * 128 + 128)):
+            t = _dec_exact(qa[m, k]) * _dec_exact(qb[n, k])
+            p += t
+            pabs += abs(t)
+        sc = Fraction(float(sa[m, kb])) * Fraction(float(sb[n, kb]))
+        total += p * sc
+        S += pabs * abs(sc)
+    return total, S
+
+
+@pytest.mark.parametrize("M,N,K", [(3, 5, 128), (2, 4, 384), (4, 3, 208)])
+def test_wgrad_fraction_brute_force(M, N, K):
+    rng = np.random.default_rng(M * 7 + N * 3 + K)
+    KB = -(-K // 128)
+    qa = rng.choice(FINITE, size=(M, K)).astype(np.uint8)
+    qb = rng.choice(FINITE, size=(N, K)).astype(np.uint8)
+    sa = rng.uniform(1e-3, 2.0, size=(M, KB)).astype(np.float32)
+    sb = rng.uniform(1e-3, 2.0, size=(N, KB)).astype(np.float32)
+    sb[rng.random(sb.shape) < 0.3] *= -1
+    c32, S = oracle.wgrad_gemm(qa, sa, qb, sb)
+    u = 2.0 ** -24
+    for m in range(M):
+        for n in range(N):
+            exact, Se = _exact_rows(qa, sa, qb, sb, m, n)
+            err = abs(Fraction(float(c32[m, n])) - exact)
+            assert err <= Fraction((KB + 3) * u * 1.0001) * Se + Fraction(2.0 ** -149)
+            assert abs(Fraction(float(S[m, n])) - Se) <= Fraction(1e-12) * Se
+    # each row of B has its own scale: rescaling row 1 of sb changes only column 1
+    sb2 = sb.copy()
+    sb2[1] *= 2
+    c2, _ = oracle.wgrad_gemm(qa, sa, qb, sb2)
+    assert np.array_equal(np.delete(c2, 1, axis=1), np.delete(c32, 1, axis=1))
+    assert np.array_equal(c2[:, 1], c32[:, 1] * 2)
+
+
+def test_wgrad_with_block_constant_row_scales_equals_block_gemm():
+    # when the 128 rows of each B block share their scales, the per-row form
+    # is the forward GEMM with 128x128 block scales, bit for bit.
+    rng = np.random.default_rng(41)
+    M, N, K = 5, 300, 256
+    qa, sa, qb, sb_blocks = _rand_case(rng, M, N, K)
+    sb_rows = np.repeat(sb_blocks, 128, axis=0)[:N]
+    c_rows, S_rows = oracle.wgrad_gemm(qa, sa, qb, sb_rows)
+    c_blk, S_blk = oracle.gemm(qa, sa, qb, sb_blocks)
+    assert np.array_equal(c_rows, c_blk) and np.array_equal(S_rows, S_blk)

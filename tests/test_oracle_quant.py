@@ -150,3 +150,71 @@ def test_threading_does_not_change_results():
     a = oracle.quant_act(_bits(x), threads=1)
     b = oracle.quant_act(_bits(x), threads=8)
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+# ---- the backward-pass layouts: 128x1 activation tiles and transposed weights
+def test_act_t_scales_are_column_maxima_over_128_rows():
+    # 128x1 tiles along M: st[k, mb] = fl32(max_{m in block mb} |x[m, k]| / 448),
+    # computed here straight from x with numpy; a ragged last block (M = 300)
+    # covers rows 256..299 only.
+    rng = np.random.default_rng(31)
+    M, K = 300, 136
+    x = _bf16(rng.standard_normal((M, K)) * np.exp2(rng.integers(-8, 8, size=(1, K))))
+    qt, st = oracle.quant_act_t(_bits(x))
+    assert qt.shape == (K, M) and st.shape == (K, 3)
+    xf = x.float().numpy()
+    for mb in range(3):
+        amax = np.abs(xf[128 * mb:min(M, 128 * mb + 128)]).max(axis=0)
+        assert np.array_equal(st[:, mb], amax.astype(np.float32) / np.float32(448))
+
+
+def test_act_t_codes_decode_to_the_transposed_input():
+    # q[k, m] * st[k, m / 128] approximates x[m, k] within half an E4M3 step
+    # of the quotient (plus the quotient's own rounding): this fails for a
+    # transposed operand or a scale taken from the wrong block.
+    rng = np.random.default_rng(32)
+    M, K = 256, 128
+    x = _bf16(rng.standard_normal((M, K)))
+    x[:, 5] *= 1000.0  # one loud column must not change its neighbours' scales
+    qt, st = oracle.quant_act_t(_bits(x))
+    xf = x.float().numpy().astype(np.float64)
+    deq = oracle.e4m3_decode(qt) * np.repeat(st.astype(np.float64), 128, axis=1)[:, :M]
+    y = xf.T / np.repeat(st.astype(np.float64), 128, axis=1)[:, :M]
+    bound = 0.5 * _e4m3_ulp(y) * np.repeat(st, 128, axis=1)[:, :M] + np.abs(xf.T) * 2.0 ** -23
+    assert np.all(np.abs(deq - xf.T) <= bound)
+    assert st[5, 0] > 100 * st[4, 0] and st[5, 1] > 100 * st[6, 1]
+
+
+def test_act_t_spike_in_one_column_and_block():
+    # a single nonzero at (m, k) = (200, 3): only tile (k = 3, mb = 1) has a
+    # nonzero scale, and its code at m = 200 is 0x7E (+448).
+    x = torch.zeros(256, 16, dtype=torch.bfloat16)
+    x[200, 3] = 7.0
+    qt, st = oracle.quant_act_t(_bits(x))
+    want_s = np.zeros((16, 2), np.float32)
+    want_s[3, 1] = np.float32(7.0) / np.float32(448)
+    assert np.array_equal(st, want_s)
+    want_q = np.zeros((16, 256), np.uint8)
+    want_q[3, 200] = 0x7E
+    assert np.array_equal(qt, want_q)
+
+
+def test_weight_t_is_the_same_blocks_in_the_other_layout():
+    # the transposed outputs hold, for code (k, n), the code of w[n, k] and the
+    # scale of block (n / 128, k / 128); checked through the block amax
+    # computed with numpy and the decode bound, not through the transpose.
+    rng = np.random.default_rng(33)
+    N, K = 320, 272
+    w = _bf16(rng.standard_normal((N, K)) * 0.02)
+    q, s, qt, st = oracle.quant_weight_t(_bits(w))
+    assert qt.shape == (K, N) and st.shape == (3, 3)
+    wf = w.float().numpy()
+    for kb in range(3):
+        for nb in range(3):
+            blk = wf[128 * nb:128 * nb + 128, 128 * kb:128 * kb + 128]
+            assert st[kb, nb] == np.float32(np.abs(blk).max()) / np.float32(448)
+    sc = np.repeat(np.repeat(st.astype(np.float64), 128, 0), 128, 1)[:K, :N]
+    deq = oracle.e4m3_decode(qt) * sc
+    y = wf.T.astype(np.float64) / sc
+    assert np.all(np.abs(deq - wf.T) <= 0.5 * _e4m3_ulp(y) * sc + np.abs(wf.T) * 2.0 ** -23)
+    assert np.array_equal(qt.T, q) and np.array_equal(st.T, s)
