@@ -22,7 +22,9 @@ struct DeviceInfo {
     bool init = false;
     bool supported = false;
     int sms = 0;
-    int pair_clusters = -1;  // co-resident 2-CTA clusters of the pair kernel (-1: not queried)
+    // co-resident 2-CTA clusters of the pair kernel, per B-scale layout
+    // ([0]: 128x128 blocks, [1]: one per row); -1: not queried yet
+    int pair_clusters[2] = {-1, -1};
 };
 
 constexpr int kMaxDevices = 64;
@@ -182,8 +184,49 @@ int fp8q_quant_weight(const void* w_bf16, int64_t N, int64_t K, void* q_e4m3, fl
     if (!make_map_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w_bf16, K, N, 128, 128,
                      CU_TENSOR_MAP_SWIZZLE_NONE))
         return FP8Q_ERR_CUDA;
-    return fp8q::launch_quant_weight(&tmW, q_e4m3, scales, N, K, stream, dev->sms, g_timeout_ns) ==
+    return fp8q::launch_quant_weight(&tmW, q_e4m3, scales, nullptr, nullptr, N, K, stream, dev->sms,
+                                     g_timeout_ns) == cudaSuccess
+               ? FP8Q_OK
+               : FP8Q_ERR_CUDA;
+}
+
+int fp8q_quant_act_t(const void* x_bf16, int64_t M, int64_t K, void* qt_e4m3, float* st,
+                     cudaStream_t stream) {
+    if (M < 0 || K <= 0 || M > kI32Max || K > kI32Max) return FP8Q_ERR_SHAPE;
+    if (M == 0) return FP8Q_OK;
+    if (!x_bf16 || !qt_e4m3 || !st) return FP8Q_ERR_NULL;
+    if (K % 16 != 0 || M % 16 != 0 || !aligned(x_bf16, 16) || !aligned(qt_e4m3, 16) ||
+        !aligned(st, 4))
+        return FP8Q_ERR_ALIGN;
+    DeviceInfo* dev = nullptr;
+    if (int rc = current_device(&dev)) return rc;
+    CUtensorMap tmX;
+    if (!make_map_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x_bf16, K, M, 128, 128,
+                     CU_TENSOR_MAP_SWIZZLE_NONE))
+        return FP8Q_ERR_CUDA;
+    return fp8q::launch_quant_act_t(&tmX, qt_e4m3, st, M, K, stream, dev->sms, g_timeout_ns) ==
                    cudaSuccess
+               ? FP8Q_OK
+               : FP8Q_ERR_CUDA;
+}
+
+int fp8q_quant_weight_t(const void* w_bf16, int64_t N, int64_t K, void* q_e4m3, float* scales,
+                        void* qt_e4m3, float* st, cudaStream_t stream) {
+    if (N < 0 || K <= 0 || N > kI32Max || K > kI32Max) return FP8Q_ERR_SHAPE;
+    if (N == 0) return FP8Q_OK;
+    if (!w_bf16 || !qt_e4m3 || !st || (q_e4m3 == nullptr) != (scales == nullptr))
+        return FP8Q_ERR_NULL;
+    if (K % 16 != 0 || N % 16 != 0 || !aligned(w_bf16, 16) || !aligned(qt_e4m3, 16) ||
+        !aligned(st, 4) || (q_e4m3 && !aligned(q_e4m3, 16)) || (scales && !aligned(scales, 4)))
+        return FP8Q_ERR_ALIGN;
+    DeviceInfo* dev = nullptr;
+    if (int rc = current_device(&dev)) return rc;
+    CUtensorMap tmW;
+    if (!make_map_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w_bf16, K, N, 128, 128,
+                     CU_TENSOR_MAP_SWIZZLE_NONE))
+        return FP8Q_ERR_CUDA;
+    return fp8q::launch_quant_weight(&tmW, q_e4m3, scales, qt_e4m3, st, N, K, stream, dev->sms,
+                                     g_timeout_ns) == cudaSuccess
                ? FP8Q_OK
                : FP8Q_ERR_CUDA;
 }
@@ -206,8 +249,14 @@ int fp8q_gather_rows(const void* q_src, const float* s_src, int64_t T, int64_t K
                : FP8Q_ERR_CUDA;
 }
 
-int fp8_block_gemm(const void* A, const float* sa, const void* B, const float* sb, void* C_bf16,
-                   int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The dense GEMM C = A * B^T; row_scaled_b selects sb [N][KB] (one scale per
+// row of B) instead of sb [ceil(N/128)][KB].
+int dense_gemm(const void* A, const float* sa, const void* B, const float* sb, void* C_bf16,
+               int64_t M, int64_t N, int64_t K, bool row_scaled_b, cudaStream_t stream) {
     if (M < 0 || N <= 0 || K <= 0 || M > kI32Max || N > kI32Max || K > kI32Max)
         return FP8Q_ERR_SHAPE;
     if (M == 0) return FP8Q_OK;
@@ -224,8 +273,9 @@ int fp8_block_gemm(const void* A, const float* sa, const void* B, const float* s
     bool pair = g_pair_mode && bn == 256 && M > 128;
     if (pair) {
         std::lock_guard<std::mutex> lock(g_mutex);
-        if (dev->pair_clusters < 0) dev->pair_clusters = fp8q::gemm_pair_max_clusters(256);
-        pair = dev->pair_clusters > 0;
+        int& pc = dev->pair_clusters[row_scaled_b ? 1 : 0];
+        if (pc < 0) pc = fp8q::gemm_pair_max_clusters(256, row_scaled_b);
+        pair = pc > 0;
     }
     CUtensorMap tmA, tmB, tmC;
     if (!make_map_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, K, M, 128, 128) ||
@@ -241,6 +291,7 @@ int fp8_block_gemm(const void* A, const float* sa, const void* B, const float* s
     g.bn = bn;
     g.grouped = false;
     g.pair = pair;
+    g.row_scaled_b = row_scaled_b;
     g.stream = stream;
     fp8q::GemmArgs& a = g.args;
     a.sa = sa;
@@ -263,12 +314,27 @@ int fp8_block_gemm(const void* A, const float* sa, const void* B, const float* s
     a.timeout_ns = g_timeout_ns;
     a.debug = g_inject;
     if (pair) {
-        const int64_t clusters = units < dev->pair_clusters ? units : dev->pair_clusters;
+        const int pc = dev->pair_clusters[row_scaled_b ? 1 : 0];
+        const int64_t clusters = units < pc ? units : pc;
         g.grid = static_cast<unsigned>(2 * clusters);
     } else {
         g.grid = static_cast<unsigned>(units < dev->sms ? units : dev->sms);
     }
     return fp8q::launch_gemm(g) == cudaSuccess ? FP8Q_OK : FP8Q_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fp8_block_gemm(const void* A, const float* sa, const void* B, const float* sb, void* C_bf16,
+                   int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
+    return dense_gemm(A, sa, B, sb, C_bf16, M, N, K, false, stream);
+}
+
+int fp8_wgrad_gemm(const void* A, const float* sa, const void* B, const float* sb, void* C_bf16,
+                   int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
+    return dense_gemm(A, sa, B, sb, C_bf16, M, N, K, true, stream);
 }
 
 int fp8_grouped_gemm(const void* A, const float* sa, const void* B, const float* sb,
@@ -300,6 +366,7 @@ int fp8_grouped_gemm(const void* A, const float* sa, const void* B, const float*
     g.bn = bn;
     g.grouped = true;
     g.pair = false;
+    g.row_scaled_b = false;
     g.stream = stream;
     fp8q::GemmArgs& a = g.args;
     a.sa = sa;

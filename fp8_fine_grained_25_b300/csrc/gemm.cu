@@ -64,7 +64,9 @@ constexpr int kScaleKb = 4;     // K blocks of scales per ring slot
 constexpr int kScaleSlots = 4;  // ring slots (16 K blocks staged ahead)
 constexpr int kMaxNb = 2;       // 128-column blocks of one tile (BN <= 256, n0 % BN == 0)
 
-template <int BN, bool GROUPED, bool PAIR>
+// ROWB: B carries one scale per row (1x128 tiles, the weight-gradient GEMM)
+// instead of one per 128x128 block.
+template <int BN, bool GROUPED, bool PAIR, bool ROWB = false>
 struct Layout {
     static constexpr int A_BYTES = BM * BK;
     static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // rows of B this CTA loads
@@ -76,7 +78,9 @@ struct Layout {
     static constexpr int EPI_WARP_BYTES = 2 * EPI_BOX_BYTES;
     static constexpr int EPI_BYTES = GROUPED ? 0 : kEpiWarps * EPI_WARP_BYTES;
     // slot: sa as [128 rows][kScaleKb], then sb as [kMaxNb][kScaleKb]
-    static constexpr int SCALE_SLOT_BYTES = 4 * kScaleKb * (BM + kMaxNb);
+    // (ROWB: sb as [kScaleKb][BN], the tile's columns contiguous per K block)
+    static constexpr int SB_PER_KB = ROWB ? BN : kMaxNb;
+    static constexpr int SCALE_SLOT_BYTES = 4 * kScaleKb * (BM + SB_PER_KB);
     static constexpr int SCALE_BYTES = kScaleSlots * SCALE_SLOT_BYTES;
     static constexpr int NBUF = (512 / BN) > 4 ? 4 : (512 / BN);  // TMEM buffers of BN columns
     static constexpr int TMEM_COLS = NBUF * BN <= 128 ? 128 : NBUF * BN <= 256 ? 256 : 512;
@@ -99,6 +103,7 @@ struct Layout {
     static constexpr int CHUNKS = HALF / 32;  // 32-column TMEM loads, issued in pairs
     static_assert(BN == 128 || BN == 256, "tile width must be 128 or 256");
     static_assert(!(PAIR && GROUPED), "pair mode is for the dense GEMM");
+    static_assert(!(ROWB && GROUPED), "row-scaled B is for the dense GEMM");
     static_assert(STAGES >= 2, "not enough shared memory for two stages");
     static_assert(8 * NUM_BARS + 16 <= 512, "barrier area overflow");
     static constexpr int smem_bytes(int E) {
@@ -202,11 +207,11 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     return __all_sync(0xFFFFFFFFu, mbar_wait<CLUSTER>(bar, parity, abort_flag, limit));
 }
 
-template <int BN, bool GROUPED, bool PAIR>
+template <int BN, bool GROUPED, bool PAIR, bool ROWB>
 __global__ void __launch_bounds__(kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
-    using L = Layout<BN, GROUPED, PAIR>;
+    using L = Layout<BN, GROUPED, PAIR, ROWB>;
     constexpr int S = L::STAGES;
     constexpr int NBUF = L::NBUF;
     extern __shared__ uint8_t smem_raw[];
@@ -416,7 +421,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                         }
                     }
-                    if (lane < kMaxNb) {
+                    if constexpr (ROWB) {
+                        // sb[n][kb0 + j] -> slot float BM * kScaleKb + j * BN + (n - n0)
+                        const uint32_t sbl = sl + 4u * kScaleKb * BM;
+#pragma unroll 4
+                        for (int i = 0; i < BN / 32; ++i) {
+                            const int c = lane + 32 * i;
+                            const int n = tile.n0 + c;
+                            const bool col_ok = n < args.N;
+                            const float* src = args.sb + (col_ok ? static_cast<int64_t>(n) * KB + kb0 : 0);
+#pragma unroll
+                            for (int j = 0; j < kScaleKb; ++j) {
+                                const bool in = col_ok && kb0 + j < KB;
+                                cp_async_4(sbl + 4u * (j * BN + c), in ? src + j : args.sb, in ? 4u : 0u);
+                            }
+                        }
+                    } else if (lane < kMaxNb) {
                         const float* src = sb_e + (sb_ok ? static_cast<int64_t>(nb) * KB + kb0 : 0);
                         const uint32_t dst = sl + 16u * (BM + lane);
                         if (wide) {
@@ -466,6 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // so each K block needs one scale product sa[m][kb] * sb[nb][kb].
             const int rel_nb = (h * L::HALF) >> 7;
             float4 sa4 = make_float4(0.f, 0.f, 0.f, 0.f), sb4 = sa4;
+            const float* sb_cols = scale_ring;  // ROWB: this warp's sb columns in the slot
             for (int kb = 0; kb < KB; ++kb) {
                 const int j = kb & (kScaleKb - 1);
                 if (j == 0) {
@@ -476,12 +497,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const float* sl = scale_ring + slot * (L::SCALE_SLOT_BYTES / 4);
                     sa4 = *reinterpret_cast<const float4*>(sl + 4 * row);
-                    sb4 = *reinterpret_cast<const float4*>(sl + 4 * (BM + rel_nb));
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(L::SEMPTY + slot));
-                    if (++slot == kScaleSlots) {
-                        slot = 0;
-                        sphase ^= 1u;
+                    if constexpr (ROWB) {
+                        // read per K block below; the slot is released after
+                        // its last K block
+                        sb_cols = sl + kScaleKb * BM + h * L::HALF;
+                    } else {
+                        sb4 = *reinterpret_cast<const float4*>(sl + 4 * (BM + rel_nb));
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar(L::SEMPTY + slot));
+                        if (++slot == kScaleSlots) {
+                            slot = 0;
+                            sphase ^= 1u;
+                        }
                     }
                 }
                 const float a_s = j == 0 ? sa4.x : j == 1 ? sa4.y : j == 2 ? sa4.z : sa4.w;
@@ -500,18 +527,47 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld32(taddr + 32 * c, r0);
                     tmem_ld32(taddr + 32 * (c + 1), r1);
                     tmem_wait_ld64(r0, r1);
+                    if constexpr (ROWB) {
+                        // column n's scale product is sa[m][kb] * sb[n][kb]
+                        const float* sbk = sb_cols + j * BN + 32 * c;
 #pragma unroll
-                    for (int i = 0; i < 32; i += 2)
-                        ffma2(acc[32 * c + i], acc[32 * c + i + 1], r0[i], r0[i + 1], cs);
+                        for (int i = 0; i < 32; i += 4) {
+                            const float4 b = *reinterpret_cast<const float4*>(sbk + i);
+                            ffma2_cols(acc[32 * c + i], acc[32 * c + i + 1], r0[i], r0[i + 1], a_s, b.x, b.y);
+                            ffma2_cols(acc[32 * c + i + 2], acc[32 * c + i + 3], r0[i + 2], r0[i + 3], a_s,
+                                       b.z, b.w);
+                        }
 #pragma unroll
-                    for (int i = 0; i < 32; i += 2)
-                        ffma2(acc[32 * (c + 1) + i], acc[32 * (c + 1) + i + 1], r1[i], r1[i + 1], cs);
+                        for (int i = 0; i < 32; i += 4) {
+                            const float4 b = *reinterpret_cast<const float4*>(sbk + 32 + i);
+                            ffma2_cols(acc[32 * (c + 1) + i], acc[32 * (c + 1) + i + 1], r1[i], r1[i + 1],
+                                       a_s, b.x, b.y);
+                            ffma2_cols(acc[32 * (c + 1) + i + 2], acc[32 * (c + 1) + i + 3], r1[i + 2],
+                                       r1[i + 3], a_s, b.z, b.w);
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2)
+                            ffma2(acc[32 * c + i], acc[32 * c + i + 1], r0[i], r0[i + 1], cs);
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2)
+                            ffma2(acc[32 * (c + 1) + i], acc[32 * (c + 1) + i + 1], r1[i], r1[i + 1], cs);
+                    }
                 }
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) {
                     if constexpr (PAIR) mbar_arrive_cluster(temptry_base + 8u * abuf);
                     else mbar_arrive(bar(L::TEMPTY + abuf));
+                }
+                if constexpr (ROWB) {
+                    if (j == kScaleKb - 1 || kb == KB - 1) {
+                        if (lane == 0) mbar_arrive(bar(L::SEMPTY + slot));
+                        if (++slot == kScaleSlots) {
+                            slot = 0;
+                            sphase ^= 1u;
+                        }
+                    }
                 }
                 if (++abuf == NBUF) {
                     abuf = 0;
@@ -587,9 +643,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0 && *abort_flag) atomicOr(&g_device_status, FP8Q_DEVSTATUS_TIMEOUT);
 }
 
-template <int BN, bool GROUPED, bool PAIR>
+template <int BN, bool GROUPED, bool PAIR, bool ROWB>
 cudaError_t prepare(int smem) {
-    auto kern = fp8_gemm_kernel<BN, GROUPED, PAIR>;
+    auto kern = fp8_gemm_kernel<BN, GROUPED, PAIR, ROWB>;
     // setmaxnreg.inc waits until the registers it asks for are free in the
     // CTA's launch pool; a pool smaller than the split would never satisfy
     // it, so refuse to launch in that case.
@@ -601,12 +657,12 @@ cudaError_t prepare(int smem) {
     return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
 }
 
-template <int BN, bool GROUPED, bool PAIR>
+template <int BN, bool GROUPED, bool PAIR, bool ROWB = false>
 cudaError_t launch_one(const GemmLaunch& g) {
-    using L = Layout<BN, GROUPED, PAIR>;
-    auto kern = fp8_gemm_kernel<BN, GROUPED, PAIR>;
+    using L = Layout<BN, GROUPED, PAIR, ROWB>;
+    auto kern = fp8_gemm_kernel<BN, GROUPED, PAIR, ROWB>;
     const int smem = L::smem_bytes(GROUPED ? g.args.E : 0);
-    cudaError_t err = prepare<BN, GROUPED, PAIR>(smem);
+    cudaError_t err = prepare<BN, GROUPED, PAIR, ROWB>(smem);
     if (err != cudaSuccess) return err;
     if constexpr (!PAIR) {
         kern<<<g.grid, kThreads, smem, g.stream>>>(*g.tmA, *g.tmB, *g.tmC, g.args);
@@ -628,11 +684,11 @@ cudaError_t launch_one(const GemmLaunch& g) {
     }
 }
 
-template <int BN>
+template <int BN, bool ROWB>
 int pair_max_clusters() {
-    using L = Layout<BN, false, true>;
+    using L = Layout<BN, false, true, ROWB>;
     const int smem = L::smem_bytes(0);
-    if (prepare<BN, false, true>(smem) != cudaSuccess) return 0;
+    if (prepare<BN, false, true, ROWB>(smem) != cudaSuccess) return 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
@@ -645,7 +701,7 @@ int pair_max_clusters() {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, fp8_gemm_kernel<BN, false, true>, &cfg) != cudaSuccess)
+    if (cudaOccupancyMaxActiveClusters(&n, fp8_gemm_kernel<BN, false, true, ROWB>, &cfg) != cudaSuccess)
         return 0;
     return n;
 }
@@ -660,13 +716,23 @@ int gemm_stages(int bn) {
     }
 }
 
-int gemm_pair_max_clusters(int bn) { return bn == 256 ? pair_max_clusters<256>() : 0; }
+int gemm_pair_max_clusters(int bn, bool row_scaled_b) {
+    if (bn != 256) return 0;
+    return row_scaled_b ? pair_max_clusters<256, true>() : pair_max_clusters<256, false>();
+}
 
 cudaError_t launch_gemm(const GemmLaunch& g) {
     if (g.grouped) {
+        if (g.row_scaled_b) return cudaErrorInvalidValue;
         switch (g.bn) {
             case 128: return launch_one<128, true, false>(g);
             case 256: return launch_one<256, true, false>(g);
+        }
+    } else if (g.row_scaled_b) {
+        if (g.pair) return g.bn == 256 ? launch_one<256, false, true, true>(g) : cudaErrorInvalidValue;
+        switch (g.bn) {
+            case 128: return launch_one<128, false, false, true>(g);
+            case 256: return launch_one<256, false, false, true>(g);
         }
     } else if (g.pair) {
         if (g.bn == 256) return launch_one<256, false, true>(g);

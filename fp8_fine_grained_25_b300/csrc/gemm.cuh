@@ -12,7 +12,7 @@ constexpr int kMaxExperts = 1024;
 
 struct GemmArgs {
     const float* sa;         // [M, KB]
-    const float* sb;         // [NB, KB], or [E][NB][KB] when grouped
+    const float* sb;         // [NB, KB], or [E][NB][KB] when grouped, or [N, KB] (row_scaled_b)
     __nv_bfloat16* C;        // [M, N] (written directly by the grouped epilogue)
     const int32_t* offsets;  // [E + 1], grouped only (device memory)
     int32_t M, N, K;         // M = total rows of A and C
@@ -33,6 +33,7 @@ struct GemmLaunch {
     int bn;
     bool grouped;
     bool pair;               // 2-CTA clusters with the 2-CTA MMA (dense only)
+    bool row_scaled_b;       // sb holds one scale per row of B (dense only)
     unsigned grid;           // CTAs (a multiple of 2 in pair mode)
     cudaStream_t stream;
 };
@@ -41,7 +42,7 @@ cudaError_t launch_gemm(const GemmLaunch& g);
 int gemm_stages(int bn);
 // Pair mode: how many 2-CTA clusters of the dense kernel fit on the device
 // at once (0 if none or on error).
-int gemm_pair_max_clusters(int bn);
+int gemm_pair_max_clusters(int bn, bool row_scaled_b);
 cudaError_t read_device_status(cudaStream_t stream, uint32_t* out, bool clear);
 
 }  // namespace fp8q

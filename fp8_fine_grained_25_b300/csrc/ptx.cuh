@@ -69,6 +69,23 @@ __device__ __forceinline__ void ffma2(float& a0, float& a1, uint32_t p0, uint32_
         : "r"(p0), "r"(p1), "f"(s));
 }
 
+// The same with one scale per column: (a0, a1) += (p0 * c0, p1 * c1) where
+// (c0, c1) = (s * b0, s * b1); the scale products and the FMAs are each
+// rounded to nearest.
+__device__ __forceinline__ void ffma2_cols(float& a0, float& a1, uint32_t p0, uint32_t p1, float s,
+                                           float b0, float b1) {
+    asm("{\n\t.reg .b64 a, p, s, c;\n\t"
+        "mov.b64 a, {%0, %1};\n\t"
+        "mov.b64 p, {%2, %3};\n\t"
+        "mov.b64 s, {%4, %4};\n\t"
+        "mov.b64 c, {%5, %6};\n\t"
+        "mul.rn.f32x2 c, s, c;\n\t"
+        "fma.rn.f32x2 a, p, c, a;\n\t"
+        "mov.b64 {%0, %1}, a;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "r"(p0), "r"(p1), "f"(s), "f"(b0), "f"(b1));
+}
+
 // Asynchronous 4-byte global -> shared copy; `src_bytes` = 0 writes zero
 // without reading (the address must still be a valid global address).
 __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32_t src_bytes) {

@@ -268,6 +268,12 @@ __global__ void __launch_bounds__(kActThreads, 1) quant_act_kernel(const ActArgs
 // blocks (the CTA's i-th block goes to stage i mod 4 and group i mod 2), so
 // two blocks are encoded at once. Thread i of a group owns the 16-byte
 // chunks c = i + 256 j (j = 0..7): block row c / 16, columns [8 (c % 16), +8).
+//
+// With the transposed output (TRANS), each group also writes its block's
+// codes into a shared-memory tile [128 n][128 k] (two per group, used on
+// alternate blocks), then reads it back by columns: warp w of the group
+// takes rows [16 w, 16 w + 16), lane l the 4-byte column word l, and four
+// 4x4 byte transposes turn the 16 words into 4 rows of qt, 16 bytes each.
 constexpr int kWConsumerWarps = 16;
 constexpr int kWGroups = 2;  // warp groups working on alternate blocks
 constexpr int kWGroupWarps = kWConsumerWarps / kWGroups;
@@ -275,19 +281,75 @@ constexpr int kWChunksPerThread = 2048 / (32 * kWGroupWarps);
 constexpr int kWStages = 4;
 constexpr int kWStageBytes = 128 * 128 * 2;
 constexpr int kWThreads = 32 * (1 + kWConsumerWarps);
-// barriers: full[S], empty[S], red[groups] (the per-block amax exchange)
-constexpr int kWBars = 2 * kWStages + kWGroups;
-constexpr int kWSmem = kWStages * kWStageBytes + 8 * kWBars + 16 + 2 * 4 * kWConsumerWarps + 1024;
+constexpr int kWCodeTile = 128 * 128;  // bytes of one block's codes
+// barriers: full[S], empty[S], red[groups] (the per-block amax exchange),
+// codes[groups] (TRANS: the group's code tile is complete)
+constexpr int kWBars = 2 * kWStages + 2 * kWGroups;
+constexpr int kWMiscBytes = 8 * kWBars + 16 + 2 * 4 * kWConsumerWarps;
+constexpr int kWSmem = kWStages * kWStageBytes + kWMiscBytes + 1024;
+constexpr int kWCodeOff = kWStages * kWStageBytes + (kWMiscBytes + 127) / 128 * 128;
+constexpr int kWSmemT = kWCodeOff + 2 * kWGroups * kWCodeTile + 1024;
 static_assert(kWStages % kWGroups == 0, "each group must cycle through its own stages");
 
 struct WeightArgs {
-    uint8_t* q;  // [N, K]
-    float* s;    // [NB, KB]
+    uint8_t* q;   // [N, K], or null (TRANS only)
+    float* s;     // [NB, KB], or null with q
+    uint8_t* qt;  // TRANS: [K, N]
+    float* st;    // TRANS: [KB, NB]
     int64_t N, K;
     uint32_t NB, KB;
     uint64_t timeout_ns;
 };
 
+// Four 4-byte words (rows r0..r3 of a byte matrix, column bytes 0..3) ->
+// four words holding its columns: out[i] byte j = in[j] byte i.
+__device__ __forceinline__ void transpose4x4(const uint32_t (&in)[4], uint32_t (&out)[4]) {
+    const uint32_t t0 = __byte_perm(in[0], in[1], 0x5140);  // r0b0 r1b0 r0b1 r1b1
+    const uint32_t t1 = __byte_perm(in[0], in[1], 0x7362);  // r0b2 r1b2 r0b3 r1b3
+    const uint32_t t2 = __byte_perm(in[2], in[3], 0x5140);
+    const uint32_t t3 = __byte_perm(in[2], in[3], 0x7362);
+    out[0] = __byte_perm(t0, t2, 0x5410);
+    out[1] = __byte_perm(t0, t2, 0x7632);
+    out[2] = __byte_perm(t1, t3, 0x5410);
+    out[3] = __byte_perm(t1, t3, 0x7632);
+}
+
+// The producer warp of the block quantizers: block b = (b / KB, b % KB) of a
+// 2-D bf16 map (128-row, 128-column units) as one 128x128 TMA box into the
+// stage ring, blocks blockIdx.x, + gridDim.x, ...; full[s] and empty[s] are
+// the barriers at bar_base + 8 s and bar_base + 8 (kWStages + s).
+__device__ __forceinline__ void block_producer(const CUtensorMap* tm, uint64_t nblocks, uint32_t KB,
+                                               uint32_t sbase, uint32_t bar_base,
+                                               volatile int* abort_flag, uint64_t timeout_ns) {
+    auto full = [&](int s) { return bar_base + 8u * s; };
+    auto empty = [&](int s) { return bar_base + 8u * (kWStages + s); };
+    int stage = 0;
+    uint32_t phase = 0, issued = 0;
+    for (uint64_t b = blockIdx.x; b < nblocks; b += gridDim.x) {
+        if (!warp_wait(empty(stage), phase ^ 1u, abort_flag, timeout_ns)) break;
+        const uint32_t rb = static_cast<uint32_t>(b / KB);
+        const uint32_t cb = static_cast<uint32_t>(b - static_cast<uint64_t>(rb) * KB);
+        if (elect_one()) {
+            mbar_arrive_expect_tx(full(stage), kWStageBytes);
+            tma_load_2d(sbase + stage * kWStageBytes, tm, full(stage), cb * 128, rb * 128);
+        }
+        __syncwarp();
+        ++issued;
+        if (++stage == kWStages) {
+            stage = 0;
+            phase ^= 1u;
+        }
+    }
+    // copies in flight land before the CTA may exit
+    for (int s = 0; s < kWStages; ++s) {
+        if (static_cast<uint32_t>(s) >= issued) break;
+        const uint32_t last = s + kWStages * ((issued - 1 - s) / kWStages);
+        volatile int local_flag = 0;
+        mbar_wait(full(s), (last / kWStages) & 1u, &local_flag, timeout_ns);
+    }
+}
+
+template <bool TRANS>
 __global__ void __launch_bounds__(kWThreads, 1)
     quant_weight_kernel(const __grid_constant__ CUtensorMap tmW, const WeightArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -298,7 +360,10 @@ __global__ void __launch_bounds__(kWThreads, 1)
     auto full = [&](int s) { return bar_base + 8u * s; };
     auto empty = [&](int s) { return bar_base + 8u * (kWStages + s); };
     auto red_bar = [&](int g) { return bar_base + 8u * (2 * kWStages + g); };
+    auto codes_bar = [&](int g) { return bar_base + 8u * (2 * kWStages + kWGroups + g); };
     uint8_t* misc = smem_raw + pad + kWStages * kWStageBytes + 8 * kWBars;
+    // TRANS: code tiles [group][2][128 x 128], after the barriers and misc
+    const uint32_t code_base = sbase + kWCodeOff;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc);
     float* red = reinterpret_cast<float*>(misc + 16);  // [2][kWConsumerWarps]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -309,7 +374,10 @@ __global__ void __launch_bounds__(kWThreads, 1)
             mbar_init(full(s), 1);
             mbar_init(empty(s), kWGroupWarps);
         }
-        for (int g = 0; g < kWGroups; ++g) mbar_init(red_bar(g), kWGroupWarps);
+        for (int g = 0; g < kWGroups; ++g) {
+            mbar_init(red_bar(g), kWGroupWarps);
+            mbar_init(codes_bar(g), kWGroupWarps);
+        }
         *abort_flag = 0;
         fence_barrier_init();
         fence_proxy_async_smem();
@@ -318,29 +386,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
     __syncthreads();
 
     if (warp == 0) {
-        int stage = 0;
-        uint32_t phase = 0, issued = 0;
-        for (uint64_t b = blockIdx.x; b < nblocks; b += gridDim.x) {
-            if (!warp_wait(empty(stage), phase ^ 1u, abort_flag, a.timeout_ns)) break;
-            const uint32_t nb = static_cast<uint32_t>(b / a.KB);
-            const uint32_t kb = static_cast<uint32_t>(b - static_cast<uint64_t>(nb) * a.KB);
-            if (elect_one()) {
-                mbar_arrive_expect_tx(full(stage), kWStageBytes);
-                tma_load_2d(sbase + stage * kWStageBytes, &tmW, full(stage), kb * 128, nb * 128);
-            }
-            __syncwarp();
-            ++issued;
-            if (++stage == kWStages) {
-                stage = 0;
-                phase ^= 1u;
-            }
-        }
-        for (int s = 0; s < kWStages; ++s) {
-            if (static_cast<uint32_t>(s) >= issued) break;
-            const uint32_t last = s + kWStages * ((issued - 1 - s) / kWStages);
-            volatile int local_flag = 0;
-            mbar_wait(full(s), (last / kWStages) & 1u, &local_flag, a.timeout_ns);
-        }
+        block_producer(&tmW, nblocks, a.KB, sbase, bar_base, abort_flag, a.timeout_ns);
     } else {
         const int cw = warp - 1;
         const int grp = cw / kWGroupWarps, gw = cw % kWGroupWarps;
@@ -384,13 +430,190 @@ __global__ void __launch_bounds__(kWThreads, 1)
             const float r = fast ? __frcp_rn(sc) : 0.0f;
             const int64_t k = static_cast<int64_t>(kb) * 128 + 8 * (tid & 15u);
             const int64_t n0 = static_cast<int64_t>(nb) * 128 + (tid >> 4);
+            // this group's code tile for this block (TRANS)
+            const uint32_t ct = code_base + (2 * grp + (iter & 1u)) * kWCodeTile;
 #pragma unroll
             for (int j = 0; j < kWChunksPerThread; ++j) {
                 const int64_t n = n0 + (kStride / 16) * j;
-                if (n < a.N && k < a.K)
-                    *reinterpret_cast<uint2*>(a.q + n * a.K + k) = encode8_r(v[j], sc, r, fast);
+                const uint2 code = encode8_r(v[j], sc, r, fast);
+                if (a.q != nullptr && n < a.N && k < a.K)
+                    *reinterpret_cast<uint2*>(a.q + n * a.K + k) = code;
+                if constexpr (TRANS) {
+                    // tile row (tid >> 4) + 16 j, bytes 8 (tid & 15) .. + 7
+                    const uint32_t off = 128u * ((tid >> 4) + (kStride / 16) * j) + 8u * (tid & 15u);
+                    asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(ct + off), "r"(code.x),
+                                 "r"(code.y)
+                                 : "memory");
+                }
             }
-            if (tid == 0) a.s[b] = sc;
+            if (tid == 0) {
+                if (a.s != nullptr) a.s[b] = sc;
+                if constexpr (TRANS) a.st[static_cast<uint64_t>(kb) * a.NB + nb] = sc;
+            }
+            if constexpr (TRANS) {
+                // All of the group's codes are in the tile once every warp has
+                // arrived; the tile used two blocks ago is free, because every
+                // warp passed this block's amax exchange after its last read.
+                __syncwarp();
+                if (lane == 0) mbar_arrive(codes_bar(grp));
+                if (!warp_wait(codes_bar(grp), iter & 1u, abort_flag, a.timeout_ns)) break;
+                const int64_t nrow = static_cast<int64_t>(nb) * 128 + 16 * gw;  // first n of the warp
+                uint32_t cols[4][4];  // [row quad][k byte i] -> 4 codes of n = nrow + 4 quad ..
+#pragma unroll
+                for (int qd = 0; qd < 4; ++qd) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int rr = 0; rr < 4; ++rr) {
+                        const uint32_t addr = ct + 128u * (16 * gw + 4 * qd + rr) + 4u * lane;
+                        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w[rr]) : "r"(addr));
+                    }
+                    transpose4x4(w, cols[qd]);
+                }
+                if (nrow < a.N) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int64_t kk = static_cast<int64_t>(kb) * 128 + 4 * lane + i;
+                        if (kk < a.K)
+                            *reinterpret_cast<uint4*>(a.qt + kk * a.N + nrow) =
+                                make_uint4(cols[0][i], cols[1][i], cols[2][i], cols[3][i]);
+                    }
+                }
+            }
+            stage += kWGroups;
+            if (stage >= kWStages) {
+                stage -= kWStages;
+                phase ^= 1u;
+            }
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && *abort_flag) atomicOr(&g_quant_status, FP8Q_DEVSTATUS_TIMEOUT);
+}
+
+// ------------------------------------------------- activations, transposed
+// 128x1 tiles (one column, 128 consecutive rows): block (mb, kb) of x [M, K]
+// is one 128x128 TMA box holding 128 tiles, one per column. In a group, lane
+// l of warp w takes the column pair p = l + 32 (w & 1) (columns 2p, 2p + 1)
+// over the rows [32 (w >> 1), +32): one 4-byte word per row, so each
+// warp-wide load reads 32 consecutive words of one row. The four row
+// segments' column maxima meet in shared memory; each thread then encodes
+// its 2 x 32 values and writes 32 bytes into each of two rows of qt.
+struct ActTArgs {
+    uint8_t* qt;  // [K, M]
+    float* st;    // [K, MB]
+    int64_t M, K;
+    uint32_t MB, KB;
+    uint64_t timeout_ns;
+};
+
+constexpr int kTRedWords = 2 * 4 * 64;  // per group: [parity][row segment][column pair]
+constexpr int kTMiscBytes = 8 * kWBars + 16 + kWGroups * kTRedWords * 4;
+constexpr int kTSmem = kWStages * kWStageBytes + kTMiscBytes + 1024;
+
+// 32 values of one tile column (bf16 in the low or high half of w[r]) with
+// scale s and reciprocal r (0: the IEEE-divide range) -> 32 codes, row order.
+template <bool HI>
+__device__ __forceinline__ void encode_col32(const uint32_t (&w)[32], float s, float r, bool fast,
+                                             uint32_t (&out)[8]) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        float y[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const uint32_t v = w[4 * i + e];
+            const float f = __uint_as_float(HI ? (v & 0xFFFF0000u) : (v << 16));
+            y[e] = fast ? div_by_scale(f, s, r) : __fdiv_rn(f, s);
+        }
+        out[i] = s == 0.0f ? 0u : (e4m3x2(y[0], y[1]) | (e4m3x2(y[2], y[3]) << 16));
+    }
+}
+
+__global__ void __launch_bounds__(kWThreads, 1)
+    quant_act_t_kernel(const __grid_constant__ CUtensorMap tmX, const ActTArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+    const uint32_t sbase = raw + pad;
+    const uint32_t bar_base = sbase + kWStages * kWStageBytes;
+    auto full = [&](int s) { return bar_base + 8u * s; };
+    auto empty = [&](int s) { return bar_base + 8u * (kWStages + s); };
+    auto red_bar = [&](int g) { return bar_base + 8u * (2 * kWStages + g); };
+    uint8_t* misc = smem_raw + pad + kWStages * kWStageBytes + 8 * kWBars;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(misc);
+    uint32_t* red = reinterpret_cast<uint32_t*>(misc + 16);  // [groups][kTRedWords]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint64_t nblocks = static_cast<uint64_t>(a.MB) * a.KB;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kWStages; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), kWGroupWarps);
+        }
+        for (int g = 0; g < kWGroups; ++g) mbar_init(red_bar(g), kWGroupWarps);
+        *abort_flag = 0;
+        fence_barrier_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 0 && lane == 0) prefetch_tmap(&tmX);
+    __syncthreads();
+
+    if (warp == 0) {
+        block_producer(&tmX, nblocks, a.KB, sbase, bar_base, abort_flag, a.timeout_ns);
+    } else {
+        const int cw = warp - 1;
+        const int grp = cw / kWGroupWarps, gw = cw % kWGroupWarps;
+        const uint32_t pr = static_cast<uint32_t>(lane) + 32u * (gw & 1);  // column pair
+        const uint32_t seg = static_cast<uint32_t>(gw >> 1);               // row segment
+        uint32_t* red_g = red + grp * kTRedWords;
+        int stage = grp;
+        uint32_t phase = 0, iter = 0;
+        for (uint64_t b = blockIdx.x + static_cast<uint64_t>(grp) * gridDim.x; b < nblocks;
+             b += static_cast<uint64_t>(kWGroups) * gridDim.x, ++iter) {
+            if (!warp_wait(full(stage), phase, abort_flag, a.timeout_ns)) break;
+            const uint32_t mb = static_cast<uint32_t>(b / a.KB);
+            const uint32_t kb = static_cast<uint32_t>(b - static_cast<uint64_t>(mb) * a.KB);
+            const uint32_t st = sbase + stage * kWStageBytes + 256u * 32u * seg + 4u * pr;
+            uint32_t w[32];
+#pragma unroll
+            for (int r = 0; r < 32; ++r)
+                asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w[r]) : "r"(st + 256u * r));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty(stage));
+            uint32_t mx = 0;
+#pragma unroll
+            for (int r = 0; r < 32; ++r) mx = __vmaxu2(mx, w[r] & 0x7FFF7FFFu);
+            // column maxima across the four row segments (halves of red_g
+            // alternate per block, as in the weight kernel's exchange)
+            uint32_t* rb = red_g + (iter & 1u) * (kTRedWords / 2);
+            rb[64 * seg + pr] = mx;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(red_bar(grp));
+            if (!warp_wait(red_bar(grp), iter & 1u, abort_flag, a.timeout_ns)) break;
+            const uint32_t m2 = __vmaxu2(__vmaxu2(rb[pr], rb[64 + pr]), __vmaxu2(rb[128 + pr], rb[192 + pr]));
+            const float amax0 = __uint_as_float(m2 << 16), amax1 = __uint_as_float(m2 & 0xFFFF0000u);
+            const float s0 = tile_scale(amax0), s1 = tile_scale(amax1);
+            const bool fast0 = amax0 >= kFastDivMinAmax, fast1 = amax1 >= kFastDivMinAmax;
+            const float r0 = fast0 ? __frcp_rn(s0) : 0.0f, r1 = fast1 ? __frcp_rn(s1) : 0.0f;
+            uint32_t c0[8], c1[8];
+            encode_col32<false>(w, s0, r0, fast0, c0);
+            encode_col32<true>(w, s1, r1, fast1, c1);
+            const int64_t k = static_cast<int64_t>(kb) * 128 + 2 * pr;
+            const int64_t m0 = static_cast<int64_t>(mb) * 128 + 32 * seg;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {  // 16 rows each (M % 16 == 0)
+                if (m0 + 16 * h < a.M) {
+                    if (k < a.K)
+                        *reinterpret_cast<uint4*>(a.qt + k * a.M + m0 + 16 * h) =
+                            make_uint4(c0[4 * h], c0[4 * h + 1], c0[4 * h + 2], c0[4 * h + 3]);
+                    if (k + 1 < a.K)
+                        *reinterpret_cast<uint4*>(a.qt + (k + 1) * a.M + m0 + 16 * h) =
+                            make_uint4(c1[4 * h], c1[4 * h + 1], c1[4 * h + 2], c1[4 * h + 3]);
+                }
+            }
+            if (seg == 0) {
+                if (k < a.K) a.st[k * a.MB + mb] = s0;
+                if (k + 1 < a.K) a.st[(k + 1) * a.MB + mb] = s1;
+            }
             stage += kWGroups;
             if (stage >= kWStages) {
                 stage -= kWStages;
@@ -480,11 +703,14 @@ cudaError_t launch_quant_act(const void* x, int64_t M, int64_t K, void* q, float
     return cudaGetLastError();
 }
 
-cudaError_t launch_quant_weight(const CUtensorMap* tmW, void* q, float* s, int64_t N, int64_t K,
-                                cudaStream_t stream, int num_sms, uint64_t timeout_ns) {
+cudaError_t launch_quant_weight(const CUtensorMap* tmW, void* q, float* s, void* qt, float* st,
+                                int64_t N, int64_t K, cudaStream_t stream, int num_sms,
+                                uint64_t timeout_ns) {
     WeightArgs a;
     a.q = static_cast<uint8_t*>(q);
     a.s = s;
+    a.qt = static_cast<uint8_t*>(qt);
+    a.st = st;
     a.N = N;
     a.K = K;
     a.NB = static_cast<uint32_t>((N + 127) / 128);
@@ -492,10 +718,36 @@ cudaError_t launch_quant_weight(const CUtensorMap* tmW, void* q, float* s, int64
     a.timeout_ns = timeout_ns;
     const uint64_t nblocks = static_cast<uint64_t>(a.NB) * a.KB;
     const unsigned grid = static_cast<unsigned>(nblocks < static_cast<uint64_t>(num_sms) ? nblocks : num_sms);
+    if (qt != nullptr) {
+        cudaError_t err = cudaFuncSetAttribute(quant_weight_kernel<true>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, kWSmemT);
+        if (err != cudaSuccess) return err;
+        quant_weight_kernel<true><<<grid, kWThreads, kWSmemT, stream>>>(*tmW, a);
+    } else {
+        cudaError_t err = cudaFuncSetAttribute(quant_weight_kernel<false>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, kWSmem);
+        if (err != cudaSuccess) return err;
+        quant_weight_kernel<false><<<grid, kWThreads, kWSmem, stream>>>(*tmW, a);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_act_t(const CUtensorMap* tmX, void* qt, float* st, int64_t M, int64_t K,
+                               cudaStream_t stream, int num_sms, uint64_t timeout_ns) {
+    ActTArgs a;
+    a.qt = static_cast<uint8_t*>(qt);
+    a.st = st;
+    a.M = M;
+    a.K = K;
+    a.MB = static_cast<uint32_t>((M + 127) / 128);
+    a.KB = static_cast<uint32_t>((K + 127) / 128);
+    a.timeout_ns = timeout_ns;
+    const uint64_t nblocks = static_cast<uint64_t>(a.MB) * a.KB;
+    const unsigned grid = static_cast<unsigned>(nblocks < static_cast<uint64_t>(num_sms) ? nblocks : num_sms);
     cudaError_t err =
-        cudaFuncSetAttribute(quant_weight_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kWSmem);
+        cudaFuncSetAttribute(quant_act_t_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTSmem);
     if (err != cudaSuccess) return err;
-    quant_weight_kernel<<<grid, kWThreads, kWSmem, stream>>>(*tmW, a);
+    quant_act_t_kernel<<<grid, kWThreads, kTSmem, stream>>>(*tmX, a);
     return cudaGetLastError();
 }
 

@@ -23,7 +23,10 @@ lib = ctypes.CDLL(_LIB_PATH)
 _i64, _i32, _p = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p
 lib.fp8q_quant_act.argtypes = [_p, _i64, _i64, _p, _p, _p]
 lib.fp8q_quant_weight.argtypes = [_p, _i64, _i64, _p, _p, _p]
+lib.fp8q_quant_act_t.argtypes = [_p, _i64, _i64, _p, _p, _p]
+lib.fp8q_quant_weight_t.argtypes = [_p, _i64, _i64, _p, _p, _p, _p, _p]
 lib.fp8_block_gemm.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p]
+lib.fp8_wgrad_gemm.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p]
 lib.fp8q_gather_rows.argtypes = [_p, _p, _i64, _i64, _p, _i64, _p, _p, _p]
 lib.fp8q_gather_rows.restype = ctypes.c_int
 lib.fp8_grouped_gemm.argtypes = [_p, _p, _p, _p, _p, _p, _i32, _i64, _i64, _i64, _p]
@@ -38,8 +41,8 @@ lib.fp8q_set_fault_injection.argtypes = [ctypes.c_uint32]
 lib.fp8q_set_fault_injection.restype = ctypes.c_int
 lib.fp8q_status_string.argtypes = [ctypes.c_int]
 lib.fp8q_status_string.restype = ctypes.c_char_p
-for _f in ("fp8q_quant_act", "fp8q_quant_weight", "fp8_block_gemm", "fp8_grouped_gemm",
-           "fp8q_get_device_status"):
+for _f in ("fp8q_quant_act", "fp8q_quant_weight", "fp8q_quant_act_t", "fp8q_quant_weight_t",
+           "fp8_block_gemm", "fp8_wgrad_gemm", "fp8_grouped_gemm", "fp8q_get_device_status"):
     getattr(lib, _f).restype = ctypes.c_int
 
 OK, ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_DEVICE, ERR_CUDA, ERR_TIMEOUT, ERR_UNSUPPORTED, ERR_OFFSETS = range(9)
@@ -131,6 +134,42 @@ def fp8q_quant_weight(w: torch.Tensor, q: torch.Tensor | None = None,
     return q, scales
 
 
+def fp8q_quant_act_t(x: torch.Tensor, qt: torch.Tensor | None = None,
+                     st: torch.Tensor | None = None, stream=None):
+    """128x1-tile quantization of bf16 activations x [M, K] (M tokens), written
+    transposed -> (qt uint8 [K, M], st fp32 [K, ceil(M/128)]): the operand
+    layout of fp8_wgrad_gemm."""
+    M, K = x.shape
+    _need(x, "x", (torch.bfloat16,), None)
+    if qt is None:
+        qt = torch.empty((K, M), dtype=torch.uint8, device=x.device)
+    if st is None:
+        st = torch.empty((K, _cdiv(M, 128)), dtype=torch.float32, device=x.device)
+    _need(qt, "qt", CODE_DTYPES, (K, M))
+    _need(st, "st", (torch.float32,), (K, _cdiv(M, 128)))
+    _check(lib.fp8q_quant_act_t(x.data_ptr(), M, K, qt.data_ptr(), st.data_ptr(), _stream(stream)),
+           "fp8q_quant_act_t")
+    return qt, st
+
+
+def fp8q_quant_weight_t(w: torch.Tensor, with_forward: bool = True, stream=None):
+    """128x128-block quantization of bf16 weights w [N, K] in both layouts ->
+    (q [N, K], s [NB, KB], qt [K, N], st [KB, NB]); with_forward=False skips
+    q and s (returned as None)."""
+    _need(w, "w", (torch.bfloat16,), None)
+    N, K = w.shape
+    NB, KB = _cdiv(N, 128), _cdiv(K, 128)
+    dev = w.device
+    q = torch.empty((N, K), dtype=torch.uint8, device=dev) if with_forward else None
+    s = torch.empty((NB, KB), dtype=torch.float32, device=dev) if with_forward else None
+    qt = torch.empty((K, N), dtype=torch.uint8, device=dev)
+    st = torch.empty((KB, NB), dtype=torch.float32, device=dev)
+    _check(lib.fp8q_quant_weight_t(w.data_ptr(), N, K, q.data_ptr() if q is not None else None,
+                                   s.data_ptr() if s is not None else None, qt.data_ptr(),
+                                   st.data_ptr(), _stream(stream)), "fp8q_quant_weight_t")
+    return q, s, qt, st
+
+
 def fp8q_gather_rows(q_src: torch.Tensor, s_src: torch.Tensor, index: torch.Tensor,
                      q_dst: torch.Tensor | None = None, s_dst: torch.Tensor | None = None,
                      stream=None):
@@ -168,6 +207,25 @@ def fp8_block_gemm(A: torch.Tensor, sa: torch.Tensor, B: torch.Tensor, sb: torch
     _need(C, "C", (torch.bfloat16,), (M, N))
     _check(lib.fp8_block_gemm(A.data_ptr(), sa.data_ptr(), B.data_ptr(), sb.data_ptr(),
                               C.data_ptr(), M, N, K, _stream(stream)), "fp8_block_gemm")
+    return C
+
+
+def fp8_wgrad_gemm(A: torch.Tensor, sa: torch.Tensor, B: torch.Tensor, sb: torch.Tensor,
+                   C: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """C[M, N] (bf16) = A[M, K] * B[N, K]^T with one scale per row of each
+    operand per 128-wide K block (sa [M, KB], sb [N, KB]): the weight
+    gradient dW = dY^T X from fp8q_quant_act_t(dY) and fp8q_quant_act_t(X)."""
+    M, K = A.shape
+    N = B.shape[0]
+    _need(A, "A", CODE_DTYPES, (M, K))
+    _need(B, "B", CODE_DTYPES, (N, K))
+    _need(sa, "sa", (torch.float32,), (M, _cdiv(K, 128)))
+    _need(sb, "sb", (torch.float32,), (N, _cdiv(K, 128)))
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    _need(C, "C", (torch.bfloat16,), (M, N))
+    _check(lib.fp8_wgrad_gemm(A.data_ptr(), sa.data_ptr(), B.data_ptr(), sb.data_ptr(),
+                              C.data_ptr(), M, N, K, _stream(stream)), "fp8_wgrad_gemm")
     return C
 
 

@@ -98,6 +98,38 @@ FP8Q_API int fp8q_quant_weight(const void* w_bf16, int64_t N, int64_t K, void* q
                       cudaStream_t stream);
 
 /*
+ * Activation quantization for the weight gradient: 128x1 tiles (128
+ * consecutive rows of one column, i.e. 1x128 tiles along the token axis of
+ * x^T), written transposed so that the tokens become the contraction axis
+ * of fp8_wgrad_gemm. The tiling follows Fig. 7a's activation granularity
+ * with the roles of the axes swapped, the layout the backward pass needs.
+ *   x_bf16  in : bf16 [M, K] (M tokens)
+ *   qt_e4m3 out: uint8 E4M3 codes [K, M]; qt[k][m] encodes x[m][k]
+ *   st      out: fp32 [K, ceil(M/128)]; st[k][mb] = amax(|x[128mb .. 128mb+127][k]|)
+ *                / 448, over the present rows when M % 128 != 0.
+ * Codes and scales are bit-exact with quantizing x^T by fp8q_quant_act.
+ * M % 16 == 0 (the row pitch of qt) and K % 16 == 0, else FP8Q_ERR_ALIGN.
+ */
+FP8Q_API int fp8q_quant_act_t(const void* x_bf16, int64_t M, int64_t K, void* qt_e4m3, float* st,
+                              cudaStream_t stream);
+
+/*
+ * Weight quantization in 128x128 blocks with the codes also written in the
+ * transposed layout, for the input gradient of the backward pass: dX = dY W
+ * is fp8_block_gemm(quant_act(dY), qt) because a 128x128 block's scale is
+ * the same for the block transposed.
+ *   w_bf16  in : bf16 [N, K]
+ *   q_e4m3, scales out: as fp8q_quant_weight, or both NULL to skip them
+ *   qt_e4m3 out: uint8 E4M3 codes [K, N]; qt[k][n] = q[n][k]
+ *   st      out: fp32 [ceil(K/128), ceil(N/128)]; st[kb][nb] = scales[nb][kb]
+ * One pass over w writes both layouts. N % 16 == 0 (the row pitch of qt) and
+ * K % 16 == 0, else FP8Q_ERR_ALIGN; passing only one of q_e4m3 and scales
+ * gives FP8Q_ERR_NULL.
+ */
+FP8Q_API int fp8q_quant_weight_t(const void* w_bf16, int64_t N, int64_t K, void* q_e4m3,
+                                 float* scales, void* qt_e4m3, float* st, cudaStream_t stream);
+
+/*
  * Row gather of quantized activations: the MoE dispatch in FP8 (news.qq.com
  * page, "FP8 低精度训练", item "低精度存储和通信", Fig. 10: activations are
  * stored and communicated in FP8). Quantizing the T tokens once and then
@@ -147,6 +179,25 @@ FP8Q_API int fp8_block_gemm(const void* A, const float* sa, const void* B, const
 FP8Q_API int fp8_grouped_gemm(const void* A, const float* sa, const void* B, const float* sb,
                      void* C_bf16, const int32_t* expert_offsets, int32_t E, int64_t total_M,
                      int64_t N, int64_t K, cudaStream_t stream);
+
+/*
+ * The weight-gradient GEMM of the backward pass (news.qq.com page: the
+ * pipeline figure's "backward for weights" chunks, and Fig. 7, where the
+ * linear layers' GEMMs run in FP8). dW = dY^T X contracts over tokens, so
+ * both operands are activations quantized in 1x128 tiles along the token
+ * axis (fp8q_quant_act_t), and the call is C = A * B^T with one scale per
+ * row of B as well as of A:
+ *   A  in : E4M3 codes [M, K] (dY^T)     sa in: fp32 [M, ceil(K/128)]
+ *   B  in : E4M3 codes [N, K] (X^T)      sb in: fp32 [N, ceil(K/128)]
+ *   C  out: bf16 [M, N] (dW)
+ *   C[m][n] = bf16_rn( sum_kb  P_kb[m][n] * (sa[m][kb] * sb[n][kb]) ),
+ * with P_kb and the FP32 promotion as in fp8_block_gemm (K is the number of
+ * tokens here). Same alignment rules, errors and accuracy as fp8_block_gemm.
+ * The pages do not fix the weight gradient's output type; like the forward
+ * GEMM it is written in bf16.
+ */
+FP8Q_API int fp8_wgrad_gemm(const void* A, const float* sa, const void* B, const float* sb,
+                            void* C_bf16, int64_t M, int64_t N, int64_t K, cudaStream_t stream);
 
 /*
  * Synchronizes `stream`, then reads the device status word (an OR of
