@@ -153,6 +153,9 @@ def make_workload(config: int, device):
 
 
 def step_flops(w) -> float:
+    if w.X is not None:  # backward of a dense layer: the dX and dW GEMMs
+        T, N = w.A.shape
+        return 2.0 * 2.0 * T * N * w.X.shape[1]
     M, K = w.A.shape
     if w.offsets is not None:
         N = w.weights["W"].shape[1]
@@ -168,7 +171,10 @@ def args_dispatch(w) -> bool:
 
 
 class Path:
-    """The hot path on one device: buffers allocated once, one call per step."""
+    """The forward hot path on one device: buffers allocated once, one call
+    per step. inputs() / outputs() name the step's bf16 inputs and its
+    outputs; step() takes replacements for either (the end-to-end run
+    passes freshly copied inputs and its own output buffers)."""
 
     def __init__(self, w, device):
         from fp8_fine_grained_25_b300 import fp8q
@@ -198,30 +204,42 @@ class Path:
             self.qx = torch.empty((T, K), dtype=torch.uint8, device=device)
             self.sx = torch.empty((T, -(-K // 128)), dtype=torch.float32, device=device)
             self.launches_per_step += 1
+        self.flops = step_flops(w)
+        self.names = (["quant_act"] + [f"quant_weight[{n}]" for n in w.weights]
+                      + [f"gemm[{n}]" for n in w.weights])
+        self.gemm_names = [f"gemm[{n}]" for n in w.weights]
+        self.describe = (w.name + ": quant_act(A) + quant_weight(W) + "
+                         + ("grouped" if w.offsets is not None else "dense")
+                         + " block-scaled GEMM per step")
 
-    def step(self, A=None, weights=None, events=None, outs=None, stream=None):
-        """One pass of the path; `outs` optionally maps weight name -> C
-        buffer, `stream` the CUDA stream (default: the current one)."""
+    def inputs(self):
+        d = {"A": self.w.tokens if self.dispatch else self.w.A}
+        d.update(self.w.weights)
+        return d
+
+    def outputs(self):
+        return {n: self.bufs[n][2] for n in self.w.weights}
+
+    def step(self, inp=None, outs=None, events=None, stream=None):
+        """One pass of the path on `stream` (default: the current one)."""
         f = self.fp8q
-        if not self.dispatch:
-            A = self.w.A if A is None else A
-        weights = self.w.weights if weights is None else weights
+        inp = self.inputs() if inp is None else inp
+        A = inp["A"]
         rec = (lambda i: events[i].record(stream)) if events is not None else (lambda i: None)
         rec(0)
         if self.dispatch:
-            X = self.w.tokens if A is None else A
-            f.fp8q_quant_act(X, self.qx, self.sx, stream=stream)
+            f.fp8q_quant_act(A, self.qx, self.sx, stream=stream)
             f.fp8q_gather_rows(self.qx, self.sx, self.w.index, self.qa, self.sa, stream=stream)
         else:
             f.fp8q_quant_act(A, self.qa, self.sa, stream=stream)
         rec(1)
         i = 2
-        for name, W in weights.items():
+        for name in self.w.weights:
             qb, sb, _ = self.bufs[name]
-            f.fp8q_quant_weight(W, qb, sb, stream=stream)
+            f.fp8q_quant_weight(inp[name], qb, sb, stream=stream)
             rec(i)
             i += 1
-        for name in weights:
+        for name in self.w.weights:
             qb, sb, C = self.bufs[name]
             if outs is not None:
                 C = outs[name]
@@ -231,6 +249,113 @@ class Path:
                 f.fp8_block_gemm(self.qa, self.sa, qb, sb, C, stream=stream)
             rec(i)
             i += 1
+
+    def kernels(self, per):
+        """Per-kernel time and throughput from the per-launch seconds `per`."""
+        w = self.w
+        M, K = w.A.shape
+        kern = {}
+        if self.dispatch:
+            T = w.tokens.shape[0]
+            qbytes = 3 * T * K + 4 * T * -(-K // 128) + 2 * (M * K + 4 * M * -(-K // 128))
+            kern["quant_act+dispatch"] = {"ms": per["quant_act"] * 1e3,
+                                          "GB/s": qbytes / per["quant_act"] / 1e9}
+        else:
+            kern["quant_act"] = {"ms": per["quant_act"] * 1e3,
+                                 "GB/s": (3 * M * K + 4 * M * -(-K // 128)) / per["quant_act"] / 1e9}
+        for n, W in w.weights.items():
+            e = W.numel()
+            blocks = e // W.shape[-1] // 128 * -(-W.shape[-1] // 128)
+            tq = per[f"quant_weight[{n}]"]
+            kern[f"quant_weight[{n}]"] = {"ms": tq * 1e3, "GB/s": (3 * e + 4 * blocks) / tq / 1e9}
+            N = W.shape[-2]
+            tg = per[f"gemm[{n}]"]
+            kern[f"gemm[{n}]"] = {"ms": tg * 1e3, "TFLOP/s": 2.0 * M * N * K / tg / 1e12}
+        return kern
+
+
+class BackwardPath:
+    """The backward pass of a dense FP8 layer y = x W^T on one device:
+        quant_act(dY) -> qdy                      (1x128 tiles)
+        quant_weight_t(W) -> qt(W)                (128x128 blocks, transposed codes)
+        dX = fp8_block_gemm(qdy, qt(W))           (input gradient, [T, K])
+        quant_act_t(dY), quant_act_t(X)           (128x1 tiles along tokens)
+        dW = fp8_wgrad_gemm(dY^T codes, X^T codes) (weight gradient, [N, K])"""
+
+    def __init__(self, w, device):
+        from fp8_fine_grained_25_b300 import fp8q
+        self.fp8q = fp8q
+        self.w = w
+        dY, X, W = w.A, w.X, w.weights["W"]
+        T, N = dY.shape
+        K = X.shape[1]
+        e = lambda *shape, dt=torch.uint8: torch.empty(shape, dtype=dt, device=device)
+        f32 = torch.float32
+        self.qdy, self.sdy = e(T, N), e(T, -(-N // 128), dt=f32)
+        self.qwt, self.swt = e(K, N), e(-(-K // 128), -(-N // 128), dt=f32)
+        self.qdyt, self.sdyt = e(N, T), e(N, -(-T // 128), dt=f32)
+        self.qxt, self.sxt = e(K, T), e(K, -(-T // 128), dt=f32)
+        self.dX = e(T, K, dt=torch.bfloat16)
+        self.dW = e(N, K, dt=torch.bfloat16)
+        self.T, self.N, self.K = T, N, K
+        self.launches_per_step = 6
+        self.dispatch = False
+        self.flops = 2.0 * (2.0 * T * N * K)
+        self.names = ["quant_act[dY]", "quant_weight_t[W]", "gemm[dX]", "quant_act_t[dY]",
+                      "quant_act_t[X]", "gemm[dW]"]
+        self.gemm_names = ["gemm[dX]", "gemm[dW]"]
+        self.describe = (w.name + ": quant_act(dY) + quant_weight_t(W) + dX GEMM + "
+                         "quant_act_t(dY) + quant_act_t(X) + dW GEMM per step")
+
+    def inputs(self):
+        return {"dY": self.w.A, "X": self.w.X, "W": self.w.weights["W"]}
+
+    def outputs(self):
+        return {"dX": self.dX, "dW": self.dW}
+
+    def step(self, inp=None, outs=None, events=None, stream=None):
+        f = self.fp8q
+        inp = self.inputs() if inp is None else inp
+        outs = self.outputs() if outs is None else outs
+        rec = (lambda i: events[i].record(stream)) if events is not None else (lambda i: None)
+        rec(0)
+        f.fp8q_quant_act(inp["dY"], self.qdy, self.sdy, stream=stream)
+        rec(1)
+        f.fp8q_quant_weight_t(inp["W"], qt=self.qwt, st=self.swt, with_forward=False, stream=stream)
+        rec(2)
+        f.fp8_block_gemm(self.qdy, self.sdy, self.qwt, self.swt, outs["dX"], stream=stream)
+        rec(3)
+        f.fp8q_quant_act_t(inp["dY"], self.qdyt, self.sdyt, stream=stream)
+        rec(4)
+        f.fp8q_quant_act_t(inp["X"], self.qxt, self.sxt, stream=stream)
+        rec(5)
+        f.fp8_wgrad_gemm(self.qdyt, self.sdyt, self.qxt, self.sxt, outs["dW"], stream=stream)
+        rec(6)
+
+    def kernels(self, per):
+        T, N, K = self.T, self.N, self.K
+        act = lambda rows, cols: 3 * rows * cols + 4 * rows * -(-cols // 128)
+        kern = {
+            "quant_act[dY]": (per["quant_act[dY]"], act(T, N), None),
+            "quant_weight_t[W]": (per["quant_weight_t[W]"],
+                                  3 * N * K + 4 * -(-N // 128) * -(-K // 128), None),
+            "gemm[dX]": (per["gemm[dX]"], None, 2.0 * T * N * K),
+            "quant_act_t[dY]": (per["quant_act_t[dY]"], act(T, N), None),
+            "quant_act_t[X]": (per["quant_act_t[X]"], act(T, K), None),
+            "gemm[dW]": (per["gemm[dW]"], None, 2.0 * T * N * K),
+        }
+        out = {}
+        for n, (t, nbytes, fl) in kern.items():
+            out[n] = {"ms": t * 1e3}
+            if nbytes is not None:
+                out[n]["GB/s"] = nbytes / t / 1e9
+            else:
+                out[n]["TFLOP/s"] = fl / t / 1e12
+        return out
+
+
+def make_path(w, device):
+    return BackwardPath(w, device) if w.X is not None else Path(w, device)
 
 
 # --------------------------------------------------------------- CPU oracle
@@ -265,6 +390,52 @@ def oracle_sample(w, rows_a: int, rows_b: int, out_rows: int, threads: int):
     return full, desc
 
 
+def oracle_sample_backward(w, rows: int, cols: int, out_rows: int, threads: int):
+    """The same for the backward step: quant_act on `rows` rows of dY, the
+    transposed weight quantization on all of W, the dX GEMM on `out_rows`
+    output rows, quant_act_t on `cols` columns of dY and of X, and the dW
+    GEMM on out_rows x cols outputs; each part scaled by its element count."""
+    import numpy as np
+    import oracle
+    dY, X, W = w.A, w.X, w.weights["W"]
+    T, N = dY.shape
+    K = X.shape[1]
+    bits = lambda t: t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    dy_rows, dy_cols, x_cols, w_bits = bits(dY[:rows]), bits(dY[:, :cols]), bits(X[:, :cols]), bits(W)
+    t = [time.perf_counter()]
+    qdy, sdy = oracle.quant_act(dy_rows, threads=threads)
+    t.append(time.perf_counter())
+    _, _, qwt, swt = oracle.quant_weight_t(w_bits, threads=threads)
+    t.append(time.perf_counter())
+    oracle.gemm(qdy, sdy, qwt, swt, rows=np.arange(out_rows), threads=threads)
+    t.append(time.perf_counter())
+    qdyt, sdyt = oracle.quant_act_t(dy_cols, threads=threads)
+    t.append(time.perf_counter())
+    qxt, sxt = oracle.quant_act_t(x_cols, threads=threads)
+    t.append(time.perf_counter())
+    oracle.wgrad_gemm(qdyt, sdyt, qxt, sxt, rows=np.arange(out_rows), threads=threads)
+    t.append(time.perf_counter())
+    d = np.diff(t)
+    full = (d[0] * T / rows + d[1] + d[2] * T / out_rows + d[3] * N / cols + d[4] * K / cols
+            + d[5] * (N * K) / (out_rows * cols))
+    desc = (f"oracle quant_act on {rows} rows of dY, quant_weight_t on all of W, dX GEMM on "
+            f"{out_rows} rows x {K} columns, quant_act_t on {cols} columns of dY and of X, dW GEMM "
+            f"on {out_rows} x {cols} outputs; sample took {t[-1] - t[0]:.2f} s, full step "
+            "extrapolated by element counts")
+    return full, desc
+
+
+def sample_oracle(w, small: bool, threads: int):
+    """The bounded oracle sample of one step of workload w (small: the
+    reference arm's per-step sample)."""
+    if w.X is not None:
+        return oracle_sample_backward(w, rows=64 if small else 256, cols=128,
+                                      out_rows=4 if small else 32, threads=threads)
+    if small:
+        return oracle_sample(w, rows_a=64, rows_b=128, out_rows=4, threads=threads)
+    return oracle_sample(w, rows_a=256, rows_b=128, out_rows=128, threads=threads)
+
+
 def run_reference(args, rank, world):
     """The reference arm: the CPU oracle, as it stands, on this machine's cores."""
     if rank != 0:
@@ -275,7 +446,7 @@ def run_reference(args, rank, world):
     times = []
     desc = ""
     for i in range(args.warmup + args.steps):
-        full, desc = oracle_sample(w, rows_a=64, rows_b=128, out_rows=4, threads=threads)
+        full, desc = sample_oracle(w, small=True, threads=threads)
         if i >= args.warmup:
             times.append(full)
     t = statistics.median(times)
@@ -299,7 +470,7 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5, 6, 7])
+    ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5, 6, 7, 8])
     ap.add_argument("--e2e-steps", type=int, default=10)
     args = ap.parse_args()
     if args.warmup < 3:
@@ -323,8 +494,8 @@ def main():
     peaks, peak_kind = load_peaks()
 
     w = make_workload(args.config, device)
-    path = Path(w, device)
-    flops = step_flops(w)
+    path = make_path(w, device)
+    flops = path.flops
     stream = torch.cuda.current_stream()
 
     for _ in range(args.warmup):
@@ -332,7 +503,7 @@ def main():
     torch.cuda.synchronize()
     assert path.fp8q.fp8q_get_device_status() == 0
 
-    nev = 1 + path.launches_per_step
+    nev = 1 + len(path.names)
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if dist is not None:
@@ -350,28 +521,9 @@ def main():
     status = path.fp8q.fp8q_get_device_status()
 
     # per-kernel averages from the events around each launch
-    names = ["quant_act"] + [f"quant_weight[{n}]" for n in w.weights] + \
-            [f"gemm[{n}]" for n in w.weights]
     per = {n: statistics.fmean(ev[j].elapsed_time(ev[j + 1]) for ev in events) / 1e3
-           for j, n in enumerate(names)}
-
-    M, K = w.A.shape
-    kern = {}
-    if path.dispatch:
-        T = w.tokens.shape[0]
-        qbytes = 3 * T * K + 4 * T * -(-K // 128) + 2 * (M * K + 4 * M * -(-K // 128))
-        kern["quant_act+dispatch"] = {"ms": per["quant_act"] * 1e3, "GB/s": qbytes / per["quant_act"] / 1e9}
-    else:
-        kern["quant_act"] = {"ms": per["quant_act"] * 1e3,
-                             "GB/s": (3 * M * K + 4 * M * -(-K // 128)) / per["quant_act"] / 1e9}
-    for n, W in w.weights.items():
-        e = W.numel()
-        blocks = e // W.shape[-1] // 128 * -(-W.shape[-1] // 128)
-        tq = per[f"quant_weight[{n}]"]
-        kern[f"quant_weight[{n}]"] = {"ms": tq * 1e3, "GB/s": (3 * e + 4 * blocks) / tq / 1e9}
-        N = W.shape[-2]
-        tg = per[f"gemm[{n}]"]
-        kern[f"gemm[{n}]"] = {"ms": tg * 1e3, "TFLOP/s": 2.0 * M * N * K / tg / 1e12}
+           for j, n in enumerate(path.names)}
+    kern = path.kernels(per)
     for v in kern.values():
         if "GB/s" in v:
             v["frac_hbm"] = v["GB/s"] / peaks["hbm_gbs"]
@@ -379,8 +531,7 @@ def main():
     # dominant kernel: the GEMM(s). It runs inside a long back-to-back loop
     # (power-capped), so the sustained measured figure is its denominator;
     # the burst-based fraction is reported beside it.
-    gemm_names = [f"gemm[{n}]" for n in w.weights]
-    t_gemm = sum(per[n] for n in gemm_names)
+    t_gemm = sum(per[n] for n in path.gemm_names)
     sustained = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
     fp8_peak = sustained * FP8_OVER_BF16
     fp8_burst = peaks["bf16_tflops"] * FP8_OVER_BF16
@@ -399,10 +550,13 @@ def main():
                     f"{peak_kind} bf16 sustained {sustained} TFLOP/s x {FP8_OVER_BF16} "
                     f"(nominal FP8:BF16 ratio); burst {peaks['bf16_tflops']} x {FP8_OVER_BF16} = "
                     f"{fp8_burst:.1f}"}
+    if len(path.gemm_names) > 1:
+        roofline["achieved_over"] = "+".join(path.gemm_names) + " (total GEMM FLOPs / total GEMM time)"
     if w.offsets is not None:
         # the grouped GEMM streams every expert's weights once: HBM-bound
+        M = w.A.shape[0]
         wbytes = w.weights["W"].numel() + 4 * w.weights["W"].numel() // 16384
-        abytes = M * K + 2 * M * w.weights["W"].shape[1]
+        abytes = M * w.A.shape[1] + 2 * M * w.weights["W"].shape[1]
         roofline["hbm_GB/s"] = (wbytes + abytes) / t_gemm / 1e9
         roofline["hbm_frac"] = roofline["hbm_GB/s"] / peaks["hbm_gbs"]
 
@@ -410,19 +564,17 @@ def main():
     value = job_throughput(world, flops, args.steps, elapsed)
 
     # end to end through the public API: every step copies its bf16 inputs
-    # from pinned host memory and its C back to pinned host memory. Two
-    # buffer sets and three streams let the copy-in of step i+1 and the
+    # from pinned host memory and its outputs back to pinned host memory.
+    # Two buffer sets and three streams let the copy-in of step i+1 and the
     # copy-out of step i-1 overlap the compute of step i (PCIe is full
     # duplex); events order each buffer's reuse.
     e2e = None
     if args.e2e_steps > 0:
-        hostA = (w.tokens if path.dispatch else w.A).cpu().pin_memory()
-        hostW = {n: W.cpu().pin_memory() for n, W in w.weights.items()}
-        hostC = {n: torch.empty(path.bufs[n][2].shape, dtype=torch.bfloat16).pin_memory()
-                 for n in w.weights}
-        devA = [torch.empty_like(w.tokens if path.dispatch else w.A) for _ in range(2)]
-        devW = [{n: torch.empty_like(W) for n, W in w.weights.items()} for _ in range(2)]
-        devC = [{n: torch.empty_like(path.bufs[n][2]) for n in w.weights} for _ in range(2)]
+        hostI = {n: t.cpu().pin_memory() for n, t in path.inputs().items()}
+        hostO = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory()
+                 for n, t in path.outputs().items()}
+        devI = [{n: torch.empty_like(t) for n, t in path.inputs().items()} for _ in range(2)]
+        devO = [{n: torch.empty_like(t) for n, t in path.outputs().items()} for _ in range(2)]
         s_in, s_cmp, s_out = (torch.cuda.Stream(device) for _ in range(3))
         ev = lambda: torch.cuda.Event()
         in_done = [ev(), ev()]
@@ -433,18 +585,17 @@ def main():
                 b = i & 1
                 s_in.wait_event(cmp_done[b])         # step i-2 no longer reads buffer b
                 with torch.cuda.stream(s_in):
-                    devA[b].copy_(hostA, non_blocking=True)
-                    for nm in w.weights:
-                        devW[b][nm].copy_(hostW[nm], non_blocking=True)
+                    for nm in hostI:
+                        devI[b][nm].copy_(hostI[nm], non_blocking=True)
                 in_done[b].record(s_in)
                 s_cmp.wait_event(in_done[b])
-                s_cmp.wait_event(out_done[b])       # C buffer b has been copied out
-                path.step(A=devA[b], weights=devW[b], outs=devC[b], stream=s_cmp)
+                s_cmp.wait_event(out_done[b])       # output buffer b has been copied out
+                path.step(inp=devI[b], outs=devO[b], stream=s_cmp)
                 cmp_done[b].record(s_cmp)
                 s_out.wait_event(cmp_done[b])
                 with torch.cuda.stream(s_out):
-                    for nm in w.weights:
-                        hostC[nm].copy_(devC[b][nm], non_blocking=True)
+                    for nm in hostO:
+                        hostO[nm].copy_(devO[b][nm], non_blocking=True)
                 out_done[b].record(s_out)
         e2e_run(3)
         torch.cuda.synchronize()
@@ -456,27 +607,25 @@ def main():
         torch.cuda.synchronize()
         te = max_over_ranks(s0.elapsed_time(s1) / 1e3, dist, device)
         e2e = {"value": job_throughput(world, flops, args.e2e_steps, te), "unit": "TFLOP/s",
-               "h2d_bytes_per_step": hostA.numel() * 2 + sum(v.numel() * 2 for v in hostW.values()),
-               "d2h_bytes_per_step": sum(v.numel() * 2 for v in hostC.values()),
+               "h2d_bytes_per_step": sum(v.numel() * v.element_size() for v in hostI.values()),
+               "d2h_bytes_per_step": sum(v.numel() * v.element_size() for v in hostO.values()),
                "ms_per_step": te / args.e2e_steps * 1e3,
                "pipelined": "copy-in / compute / copy-out on three streams, double-buffered"}
 
     cpu = None
     if rank == 0 and world == 1:
         threads = os.cpu_count() or 1
-        full, desc = oracle_sample(w, rows_a=256, rows_b=128, out_rows=128, threads=threads)
+        full, desc = sample_oracle(w, small=False, threads=threads)
         cpu = {"value": flops / full / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                "sample": desc}
 
     if rank == 0:
-        a_bytes = w.A.numel() * 2 + sum(W.numel() * 2 for W in w.weights.values())
+        a_bytes = sum(t.numel() * t.element_size() for t in path.inputs().values())
         line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "e4m3*e4m3->f32", "data": "synthetic",
-                "config": {"workload": w.name + ": quant_act(A) + quant_weight(W) + "
-                           + ("grouped" if w.offsets is not None else "dense")
-                           + " block-scaled GEMM per step",
+                "config": {"workload": path.describe,
                            "parallelism": f"replicas x{world}",
                            "l2": f"inputs larger than L2 (bf16 inputs {a_bytes / 1e6:.0f} MB "
                                  "re-read every step)"},

@@ -22,9 +22,10 @@ struct DeviceInfo {
     bool init = false;
     bool supported = false;
     int sms = 0;
-    // co-resident 2-CTA clusters of the pair kernel, per B-scale layout
-    // ([0]: 128x128 blocks, [1]: one per row); -1: not queried yet
-    int pair_clusters[2] = {-1, -1};
+    // co-resident 2-CTA clusters of the pair kernel, per tile width
+    // ([0]: 128, [1]: 256) and B-scale layout ([0]: 128x128 blocks, [1]: one
+    // per row); -1: not queried yet
+    int pair_clusters[2][2] = {{-1, -1}, {-1, -1}};
 };
 
 constexpr int kMaxDevices = 64;
@@ -270,12 +271,12 @@ int dense_gemm(const void* A, const float* sa, const void* B, const float* sb, v
     const int bn = g_force_bn ? g_force_bn : choose_bn(M, N, dev->sms);
     // 2-CTA pairs (256 x 256 tiles over two SMs) for the 256-wide tile when
     // there are at least two m-tiles to pair.
-    bool pair = g_pair_mode && bn == 256 && M > 128;
+    bool pair = g_pair_mode && M > 128;
+    int* pc = &dev->pair_clusters[bn == 256 ? 1 : 0][row_scaled_b ? 1 : 0];
     if (pair) {
         std::lock_guard<std::mutex> lock(g_mutex);
-        int& pc = dev->pair_clusters[row_scaled_b ? 1 : 0];
-        if (pc < 0) pc = fp8q::gemm_pair_max_clusters(256, row_scaled_b);
-        pair = pc > 0;
+        if (*pc < 0) *pc = fp8q::gemm_pair_max_clusters(bn, row_scaled_b);
+        pair = *pc > 0;
     }
     CUtensorMap tmA, tmB, tmC;
     if (!make_map_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, K, M, 128, 128) ||
@@ -314,8 +315,7 @@ int dense_gemm(const void* A, const float* sa, const void* B, const float* sb, v
     a.timeout_ns = g_timeout_ns;
     a.debug = g_inject;
     if (pair) {
-        const int pc = dev->pair_clusters[row_scaled_b ? 1 : 0];
-        const int64_t clusters = units < pc ? units : pc;
+        const int64_t clusters = units < *pc ? units : *pc;
         g.grid = static_cast<unsigned>(2 * clusters);
     } else {
         g.grid = static_cast<unsigned>(units < dev->sms ? units : dev->sms);

@@ -424,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if constexpr (ROWB) {
                         // sb[n][kb0 + j] -> slot float BM * kScaleKb + j * BN + (n - n0)
                         const uint32_t sbl = sl + 4u * kScaleKb * BM;
-#pragma unroll 4
+#pragma unroll 1
                         for (int i = 0; i < BN / 32; ++i) {
                             const int c = lane + 32 * i;
                             const int n = tile.n0 + c;
@@ -521,31 +521,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after_sync();
                 const uint32_t taddr = lane_base + abuf * BN + h * L::HALF;
+                if constexpr (ROWB) {
+                    // column n's scale product is sa[m][kb] * sb[n][kb]; one
+                    // 32-column chunk at a time, its 32 sb values loaded from
+                    // shared memory while the chunk's TMEM load is in flight
+                    const uint32_t sbk = smem_u32(sb_cols + j * BN);
 #pragma unroll
-                for (int c = 0; c < L::CHUNKS; c += 2) {
-                    uint32_t r0[32], r1[32];
-                    tmem_ld32(taddr + 32 * c, r0);
-                    tmem_ld32(taddr + 32 * (c + 1), r1);
-                    tmem_wait_ld64(r0, r1);
-                    if constexpr (ROWB) {
-                        // column n's scale product is sa[m][kb] * sb[n][kb]
-                        const float* sbk = sb_cols + j * BN + 32 * c;
+                    for (int c = 0; c < L::CHUNKS; ++c) {
+                        float4 b[8];
 #pragma unroll
-                        for (int i = 0; i < 32; i += 4) {
-                            const float4 b = *reinterpret_cast<const float4*>(sbk + i);
-                            ffma2_cols(acc[32 * c + i], acc[32 * c + i + 1], r0[i], r0[i + 1], a_s, b.x, b.y);
-                            ffma2_cols(acc[32 * c + i + 2], acc[32 * c + i + 3], r0[i + 2], r0[i + 3], a_s,
-                                       b.z, b.w);
+                        for (int i = 0; i < 8; ++i) b[i] = lds_f4(sbk + 4u * (32 * c + 4 * i));
+                        uint32_t r0[32];
+                        tmem_ld32(taddr + 32 * c, r0);
+                        tmem_wait_ld32(r0);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            float* a = acc + 32 * c + 4 * i;
+                            ffma2_cols(a[0], a[1], r0[4 * i], r0[4 * i + 1], a_s, b[i].x, b[i].y);
+                            ffma2_cols(a[2], a[3], r0[4 * i + 2], r0[4 * i + 3], a_s, b[i].z, b[i].w);
                         }
+                    }
+                } else {
 #pragma unroll
-                        for (int i = 0; i < 32; i += 4) {
-                            const float4 b = *reinterpret_cast<const float4*>(sbk + 32 + i);
-                            ffma2_cols(acc[32 * (c + 1) + i], acc[32 * (c + 1) + i + 1], r1[i], r1[i + 1],
-                                       a_s, b.x, b.y);
-                            ffma2_cols(acc[32 * (c + 1) + i + 2], acc[32 * (c + 1) + i + 3], r1[i + 2],
-                                       r1[i + 3], a_s, b.z, b.w);
-                        }
-                    } else {
+                    for (int c = 0; c < L::CHUNKS; c += 2) {
+                        uint32_t r0[32], r1[32];
+                        tmem_ld32(taddr + 32 * c, r0);
+                        tmem_ld32(taddr + 32 * (c + 1), r1);
+                        tmem_wait_ld64(r0, r1);
 #pragma unroll
                         for (int i = 0; i < 32; i += 2)
                             ffma2(acc[32 * c + i], acc[32 * c + i + 1], r0[i], r0[i + 1], cs);
@@ -717,8 +719,11 @@ int gemm_stages(int bn) {
 }
 
 int gemm_pair_max_clusters(int bn, bool row_scaled_b) {
-    if (bn != 256) return 0;
-    return row_scaled_b ? pair_max_clusters<256, true>() : pair_max_clusters<256, false>();
+    switch (bn) {
+        case 128: return row_scaled_b ? pair_max_clusters<128, true>() : pair_max_clusters<128, false>();
+        case 256: return row_scaled_b ? pair_max_clusters<256, true>() : pair_max_clusters<256, false>();
+        default: return 0;
+    }
 }
 
 cudaError_t launch_gemm(const GemmLaunch& g) {
@@ -729,13 +734,22 @@ cudaError_t launch_gemm(const GemmLaunch& g) {
             case 256: return launch_one<256, true, false>(g);
         }
     } else if (g.row_scaled_b) {
-        if (g.pair) return g.bn == 256 ? launch_one<256, false, true, true>(g) : cudaErrorInvalidValue;
+        if (g.pair) {
+            switch (g.bn) {
+                case 128: return launch_one<128, false, true, true>(g);
+                case 256: return launch_one<256, false, true, true>(g);
+            }
+            return cudaErrorInvalidValue;
+        }
         switch (g.bn) {
             case 128: return launch_one<128, false, false, true>(g);
             case 256: return launch_one<256, false, false, true>(g);
         }
     } else if (g.pair) {
-        if (g.bn == 256) return launch_one<256, false, true>(g);
+        switch (g.bn) {
+            case 128: return launch_one<128, false, true>(g);
+            case 256: return launch_one<256, false, true>(g);
+        }
     } else {
         switch (g.bn) {
             case 128: return launch_one<128, false, false>(g);

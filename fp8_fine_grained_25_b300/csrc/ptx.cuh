@@ -86,6 +86,16 @@ __device__ __forceinline__ void ffma2_cols(float& a0, float& a1, uint32_t p0, ui
         : "r"(p0), "r"(p1), "f"(s), "f"(b0), "f"(b1));
 }
 
+// 16-byte shared-memory load, ordered with the other volatile asm here
+// (so that it can be issued ahead of a TMEM load it should overlap).
+__device__ __forceinline__ float4 lds_f4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
 // Asynchronous 4-byte global -> shared copy; `src_bytes` = 0 writes zero
 // without reading (the address must still be a valid global address).
 __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32_t src_bytes) {

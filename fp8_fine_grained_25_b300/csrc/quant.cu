@@ -513,18 +513,34 @@ constexpr int kTSmem = kWStages * kWStageBytes + kTMiscBytes + 1024;
 // 32 values of one tile column (bf16 in the low or high half of w[r]) with
 // scale s and reciprocal r (0: the IEEE-divide range) -> 32 codes, row order.
 template <bool HI>
+__device__ __forceinline__ float col_value(uint32_t v) {
+    return __uint_as_float(HI ? (v & 0xFFFF0000u) : (v << 16));
+}
+
+template <bool HI>
 __device__ __forceinline__ void encode_col32(const uint32_t (&w)[32], float s, float r, bool fast,
                                              uint32_t (&out)[8]) {
+    if (s == 0.0f) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        float y[4];
+        for (int i = 0; i < 8; ++i) out[i] = 0u;
+    } else if (fast) {  // one branch per column, not per element
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const uint32_t v = w[4 * i + e];
-            const float f = __uint_as_float(HI ? (v & 0xFFFF0000u) : (v << 16));
-            y[e] = fast ? div_by_scale(f, s, r) : __fdiv_rn(f, s);
+        for (int i = 0; i < 8; ++i) {
+            const float y0 = div_by_scale(col_value<HI>(w[4 * i]), s, r);
+            const float y1 = div_by_scale(col_value<HI>(w[4 * i + 1]), s, r);
+            const float y2 = div_by_scale(col_value<HI>(w[4 * i + 2]), s, r);
+            const float y3 = div_by_scale(col_value<HI>(w[4 * i + 3]), s, r);
+            out[i] = e4m3x2(y0, y1) | (e4m3x2(y2, y3) << 16);
         }
-        out[i] = s == 0.0f ? 0u : (e4m3x2(y[0], y[1]) | (e4m3x2(y[2], y[3]) << 16));
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float y0 = __fdiv_rn(col_value<HI>(w[4 * i]), s);
+            const float y1 = __fdiv_rn(col_value<HI>(w[4 * i + 1]), s);
+            const float y2 = __fdiv_rn(col_value<HI>(w[4 * i + 2]), s);
+            const float y3 = __fdiv_rn(col_value<HI>(w[4 * i + 3]), s);
+            out[i] = e4m3x2(y0, y1) | (e4m3x2(y2, y3) << 16);
+        }
     }
 }
 

@@ -152,7 +152,9 @@ def fp8q_quant_act_t(x: torch.Tensor, qt: torch.Tensor | None = None,
     return qt, st
 
 
-def fp8q_quant_weight_t(w: torch.Tensor, with_forward: bool = True, stream=None):
+def fp8q_quant_weight_t(w: torch.Tensor, q: torch.Tensor | None = None,
+                        scales: torch.Tensor | None = None, qt: torch.Tensor | None = None,
+                        st: torch.Tensor | None = None, with_forward: bool = True, stream=None):
     """128x128-block quantization of bf16 weights w [N, K] in both layouts ->
     (q [N, K], s [NB, KB], qt [K, N], st [KB, NB]); with_forward=False skips
     q and s (returned as None)."""
@@ -160,14 +162,22 @@ def fp8q_quant_weight_t(w: torch.Tensor, with_forward: bool = True, stream=None)
     N, K = w.shape
     NB, KB = _cdiv(N, 128), _cdiv(K, 128)
     dev = w.device
-    q = torch.empty((N, K), dtype=torch.uint8, device=dev) if with_forward else None
-    s = torch.empty((NB, KB), dtype=torch.float32, device=dev) if with_forward else None
-    qt = torch.empty((K, N), dtype=torch.uint8, device=dev)
-    st = torch.empty((KB, NB), dtype=torch.float32, device=dev)
+    if with_forward:
+        q = torch.empty((N, K), dtype=torch.uint8, device=dev) if q is None else q
+        scales = torch.empty((NB, KB), dtype=torch.float32, device=dev) if scales is None else scales
+        _need(q, "q", CODE_DTYPES, (N, K))
+        _need(scales, "scales", (torch.float32,), (NB, KB))
+    else:
+        q = scales = None
+    qt = torch.empty((K, N), dtype=torch.uint8, device=dev) if qt is None else qt
+    st = torch.empty((KB, NB), dtype=torch.float32, device=dev) if st is None else st
+    _need(qt, "qt", CODE_DTYPES, (K, N))
+    _need(st, "st", (torch.float32,), (KB, NB))
     _check(lib.fp8q_quant_weight_t(w.data_ptr(), N, K, q.data_ptr() if q is not None else None,
-                                   s.data_ptr() if s is not None else None, qt.data_ptr(),
-                                   st.data_ptr(), _stream(stream)), "fp8q_quant_weight_t")
-    return q, s, qt, st
+                                   scales.data_ptr() if scales is not None else None,
+                                   qt.data_ptr(), st.data_ptr(), _stream(stream)),
+           "fp8q_quant_weight_t")
+    return q, scales, qt, st
 
 
 def fp8q_gather_rows(q_src: torch.Tensor, s_src: torch.Tensor, index: torch.Tensor,

@@ -78,6 +78,7 @@ class Workload:
     note: str = ""
     tokens: torch.Tensor | None = None    # MoE: the un-gathered token activations [T, K]
     index: torch.Tensor | None = None     # MoE: int32 token of each routed row (A = tokens[index])
+    X: torch.Tensor | None = None         # backward: the layer input [T, K] (A holds dY [T, N])
 
 
 def tiny(seed: int = 0, device="cpu") -> Workload:
@@ -148,5 +149,16 @@ def large_m(seed: int = 0, device="cpu", M: int = 32768) -> Workload:
                     {"B": normal_bf16((18432, HIDDEN), 0.01, seed * 1000 + 2, device)})
 
 
+def dense_backward(seed: int = 0, device="cpu", T: int = 8192) -> Workload:
+    """The backward pass of the dense 7168-square layer y = x W^T: layer input
+    X [T, 7168] ~ N(0,1) with the outlier channels (as dense_square's A),
+    output gradient dY [T, 7168] ~ N(0,1), W [7168, 7168] ~ N(0, 0.01^2)."""
+    X = activations_with_outliers(T, HIDDEN, seed * 1000 + 1, device)
+    W = normal_bf16((HIDDEN, HIDDEN), 0.01, seed * 1000 + 2, device)
+    dY = normal_bf16((T, HIDDEN), 1.0, seed * 1000 + 3, device)
+    return Workload(f"dense backward {T}x7168x7168 (dX and dW)", dY, {"W": W},
+                    note="A holds dY; X is the layer input", X=X)
+
+
 CONFIGS = {1: tiny, 2: mla_down, 3: dense_square, 4: moe_grouped, 5: large_m, 6: mla_down_fused,
-           7: moe_dispatch_fp8}
+           7: moe_dispatch_fp8, 8: dense_backward}

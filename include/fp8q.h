@@ -223,11 +223,11 @@ FP8Q_API void fp8q_set_wait_timeout_ns(uint64_t ns);
 FP8Q_API int fp8q_set_gemm_tile_n(int bn);
 
 /*
- * Whether fp8_block_gemm may run a 256 x 256 output tile on a pair of SMs
- * (2-CTA clusters with the 2-CTA tensor-core MMA, each SM holding half of
- * the B tile). 1 (the default) uses pairs when the tile width is 256 and
- * M > 128; 0 keeps one SM per 128 x N tile. Affects speed only, never
- * results. Returns FP8Q_OK.
+ * Whether fp8_block_gemm and fp8_wgrad_gemm may run an output tile of
+ * 256 rows on a pair of SMs (2-CTA clusters with the 2-CTA tensor-core MMA,
+ * each SM holding half of the B tile). 1 (the default) uses pairs whenever
+ * M > 128, for both tile widths; 0 keeps one SM per 128 x N tile. Affects
+ * speed only, never results. Returns FP8Q_OK.
  */
 FP8Q_API int fp8q_set_gemm_pairs(int enable);
 
