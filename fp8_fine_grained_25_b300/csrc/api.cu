@@ -185,7 +185,7 @@ int fp8q_quant_weight(const void* w_bf16, int64_t N, int64_t K, void* q_e4m3, fl
     if (!make_map_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w_bf16, K, N, 128, 128,
                      CU_TENSOR_MAP_SWIZZLE_NONE))
         return FP8Q_ERR_CUDA;
-    return fp8q::launch_quant_weight(&tmW, q_e4m3, scales, nullptr, nullptr, N, K, stream, dev->sms,
+    return fp8q::launch_quant_weight(&tmW, q_e4m3, scales, N, K, stream, dev->sms,
                                      g_timeout_ns) == cudaSuccess
                ? FP8Q_OK
                : FP8Q_ERR_CUDA;
@@ -201,12 +201,8 @@ int fp8q_quant_act_t(const void* x_bf16, int64_t M, int64_t K, void* qt_e4m3, fl
         return FP8Q_ERR_ALIGN;
     DeviceInfo* dev = nullptr;
     if (int rc = current_device(&dev)) return rc;
-    CUtensorMap tmX;
-    if (!make_map_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x_bf16, K, M, 128, 128,
-                     CU_TENSOR_MAP_SWIZZLE_NONE))
-        return FP8Q_ERR_CUDA;
-    return fp8q::launch_quant_act_t(&tmX, qt_e4m3, st, M, K, stream, dev->sms, g_timeout_ns) ==
-                   cudaSuccess
+    if (cdiv(M, 128) * cdiv(K, 128) > kI32Max) return FP8Q_ERR_SHAPE;
+    return fp8q::launch_quant_act_t(x_bf16, qt_e4m3, st, M, K, stream, dev->sms) == cudaSuccess
                ? FP8Q_OK
                : FP8Q_ERR_CUDA;
 }
@@ -222,12 +218,9 @@ int fp8q_quant_weight_t(const void* w_bf16, int64_t N, int64_t K, void* q_e4m3, 
         return FP8Q_ERR_ALIGN;
     DeviceInfo* dev = nullptr;
     if (int rc = current_device(&dev)) return rc;
-    CUtensorMap tmW;
-    if (!make_map_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w_bf16, K, N, 128, 128,
-                     CU_TENSOR_MAP_SWIZZLE_NONE))
-        return FP8Q_ERR_CUDA;
-    return fp8q::launch_quant_weight(&tmW, q_e4m3, scales, qt_e4m3, st, N, K, stream, dev->sms,
-                                     g_timeout_ns) == cudaSuccess
+    if (cdiv(N, 128) * cdiv(K, 128) > kI32Max) return FP8Q_ERR_SHAPE;
+    return fp8q::launch_quant_weight_t(w_bf16, q_e4m3, scales, qt_e4m3, st, N, K, stream, dev->sms) ==
+                   cudaSuccess
                ? FP8Q_OK
                : FP8Q_ERR_CUDA;
 }

@@ -1,12 +1,18 @@
 // Fine-grained FP8 quantizers: activations per 1x128 tile, weights per
 // 128x128 block (news.qq.com/rain/a/20241229A05OQF00, "FP8 低精度训练",
-// item "细粒度量化", Fig. 7a; developer.aliyun.com/article/1776647 §4.1).
+// item "细粒度量化", Fig. 7a; developer.aliyun.com/article/1776647 §4.1), and
+// the transposed layouts the backward GEMMs read.
 //
-// Both are HBM-bound streams: 2 bytes read and 1 byte written per element
-// plus one fp32 scale per tile/block. A producer warp streams the input into
-// a ring of shared-memory stages with bulk copies (TMA), so the bytes in
-// flight do not depend on registers; consumer warps read a stage, reduce the
-// amax, encode, and store codes (8-byte vectors) and scales to global memory.
+// All are HBM-bound streams: 2 bytes read and 1 byte written per element
+// (2 for both layouts) plus one fp32 scale per tile/block.
+//  - Row-major outputs (quant_act, quant_weight): a producer warp streams the
+//    input into a ring of shared-memory stages with bulk copies (TMA), so the
+//    bytes in flight do not depend on registers; consumer warps read a stage,
+//    reduce the amax, encode, and store codes and scales.
+//  - Transposed outputs (quant_act_t, quant_weight_t): persistent CTAs read
+//    128x128 blocks straight into registers (the next block's loads in flight
+//    while the current one is encoded) and write 16-byte runs of the
+//    transposed codes; the block order keeps those runs adjacent.
 //
 // Arithmetic per tile (bit-exact with the definition):
 //   amax  = max |x|                 (bf16 -> fp32 is exact, max is exact)
@@ -268,12 +274,6 @@ __global__ void __launch_bounds__(kActThreads, 1) quant_act_kernel(const ActArgs
 // blocks (the CTA's i-th block goes to stage i mod 4 and group i mod 2), so
 // two blocks are encoded at once. Thread i of a group owns the 16-byte
 // chunks c = i + 256 j (j = 0..7): block row c / 16, columns [8 (c % 16), +8).
-//
-// With the transposed output (TRANS), each group also writes its block's
-// codes into a shared-memory tile [128 n][128 k] (two per group, used on
-// alternate blocks), then reads it back by columns: warp w of the group
-// takes rows [16 w, 16 w + 16), lane l the 4-byte column word l, and four
-// 4x4 byte transposes turn the 16 words into 4 rows of qt, 16 bytes each.
 constexpr int kWConsumerWarps = 16;
 constexpr int kWGroups = 2;  // warp groups working on alternate blocks
 constexpr int kWGroupWarps = kWConsumerWarps / kWGroups;
@@ -281,75 +281,19 @@ constexpr int kWChunksPerThread = 2048 / (32 * kWGroupWarps);
 constexpr int kWStages = 4;
 constexpr int kWStageBytes = 128 * 128 * 2;
 constexpr int kWThreads = 32 * (1 + kWConsumerWarps);
-constexpr int kWCodeTile = 128 * 128;  // bytes of one block's codes
-// barriers: full[S], empty[S], red[groups] (the per-block amax exchange),
-// codes[groups] (TRANS: the group's code tile is complete)
-constexpr int kWBars = 2 * kWStages + 2 * kWGroups;
-constexpr int kWMiscBytes = 8 * kWBars + 16 + 2 * 4 * kWConsumerWarps;
-constexpr int kWSmem = kWStages * kWStageBytes + kWMiscBytes + 1024;
-constexpr int kWCodeOff = kWStages * kWStageBytes + (kWMiscBytes + 127) / 128 * 128;
-constexpr int kWSmemT = kWCodeOff + 2 * kWGroups * kWCodeTile + 1024;
+// barriers: full[S], empty[S], red[groups] (the per-block amax exchange)
+constexpr int kWBars = 2 * kWStages + kWGroups;
+constexpr int kWSmem = kWStages * kWStageBytes + 8 * kWBars + 16 + 2 * 4 * kWConsumerWarps + 1024;
 static_assert(kWStages % kWGroups == 0, "each group must cycle through its own stages");
 
 struct WeightArgs {
-    uint8_t* q;   // [N, K], or null (TRANS only)
-    float* s;     // [NB, KB], or null with q
-    uint8_t* qt;  // TRANS: [K, N]
-    float* st;    // TRANS: [KB, NB]
+    uint8_t* q;  // [N, K]
+    float* s;    // [NB, KB]
     int64_t N, K;
     uint32_t NB, KB;
     uint64_t timeout_ns;
 };
 
-// Four 4-byte words (rows r0..r3 of a byte matrix, column bytes 0..3) ->
-// four words holding its columns: out[i] byte j = in[j] byte i.
-__device__ __forceinline__ void transpose4x4(const uint32_t (&in)[4], uint32_t (&out)[4]) {
-    const uint32_t t0 = __byte_perm(in[0], in[1], 0x5140);  // r0b0 r1b0 r0b1 r1b1
-    const uint32_t t1 = __byte_perm(in[0], in[1], 0x7362);  // r0b2 r1b2 r0b3 r1b3
-    const uint32_t t2 = __byte_perm(in[2], in[3], 0x5140);
-    const uint32_t t3 = __byte_perm(in[2], in[3], 0x7362);
-    out[0] = __byte_perm(t0, t2, 0x5410);
-    out[1] = __byte_perm(t0, t2, 0x7632);
-    out[2] = __byte_perm(t1, t3, 0x5410);
-    out[3] = __byte_perm(t1, t3, 0x7632);
-}
-
-// The producer warp of the block quantizers: block b = (b / KB, b % KB) of a
-// 2-D bf16 map (128-row, 128-column units) as one 128x128 TMA box into the
-// stage ring, blocks blockIdx.x, + gridDim.x, ...; full[s] and empty[s] are
-// the barriers at bar_base + 8 s and bar_base + 8 (kWStages + s).
-__device__ __forceinline__ void block_producer(const CUtensorMap* tm, uint64_t nblocks, uint32_t KB,
-                                               uint32_t sbase, uint32_t bar_base,
-                                               volatile int* abort_flag, uint64_t timeout_ns) {
-    auto full = [&](int s) { return bar_base + 8u * s; };
-    auto empty = [&](int s) { return bar_base + 8u * (kWStages + s); };
-    int stage = 0;
-    uint32_t phase = 0, issued = 0;
-    for (uint64_t b = blockIdx.x; b < nblocks; b += gridDim.x) {
-        if (!warp_wait(empty(stage), phase ^ 1u, abort_flag, timeout_ns)) break;
-        const uint32_t rb = static_cast<uint32_t>(b / KB);
-        const uint32_t cb = static_cast<uint32_t>(b - static_cast<uint64_t>(rb) * KB);
-        if (elect_one()) {
-            mbar_arrive_expect_tx(full(stage), kWStageBytes);
-            tma_load_2d(sbase + stage * kWStageBytes, tm, full(stage), cb * 128, rb * 128);
-        }
-        __syncwarp();
-        ++issued;
-        if (++stage == kWStages) {
-            stage = 0;
-            phase ^= 1u;
-        }
-    }
-    // copies in flight land before the CTA may exit
-    for (int s = 0; s < kWStages; ++s) {
-        if (static_cast<uint32_t>(s) >= issued) break;
-        const uint32_t last = s + kWStages * ((issued - 1 - s) / kWStages);
-        volatile int local_flag = 0;
-        mbar_wait(full(s), (last / kWStages) & 1u, &local_flag, timeout_ns);
-    }
-}
-
-template <bool TRANS>
 __global__ void __launch_bounds__(kWThreads, 1)
     quant_weight_kernel(const __grid_constant__ CUtensorMap tmW, const WeightArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -360,10 +304,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
     auto full = [&](int s) { return bar_base + 8u * s; };
     auto empty = [&](int s) { return bar_base + 8u * (kWStages + s); };
     auto red_bar = [&](int g) { return bar_base + 8u * (2 * kWStages + g); };
-    auto codes_bar = [&](int g) { return bar_base + 8u * (2 * kWStages + kWGroups + g); };
     uint8_t* misc = smem_raw + pad + kWStages * kWStageBytes + 8 * kWBars;
-    // TRANS: code tiles [group][2][128 x 128], after the barriers and misc
-    const uint32_t code_base = sbase + kWCodeOff;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc);
     float* red = reinterpret_cast<float*>(misc + 16);  // [2][kWConsumerWarps]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -374,10 +315,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
             mbar_init(full(s), 1);
             mbar_init(empty(s), kWGroupWarps);
         }
-        for (int g = 0; g < kWGroups; ++g) {
-            mbar_init(red_bar(g), kWGroupWarps);
-            mbar_init(codes_bar(g), kWGroupWarps);
-        }
+        for (int g = 0; g < kWGroups; ++g) mbar_init(red_bar(g), kWGroupWarps);
         *abort_flag = 0;
         fence_barrier_init();
         fence_proxy_async_smem();
@@ -386,7 +324,29 @@ __global__ void __launch_bounds__(kWThreads, 1)
     __syncthreads();
 
     if (warp == 0) {
-        block_producer(&tmW, nblocks, a.KB, sbase, bar_base, abort_flag, a.timeout_ns);
+        int stage = 0;
+        uint32_t phase = 0, issued = 0;
+        for (uint64_t b = blockIdx.x; b < nblocks; b += gridDim.x) {
+            if (!warp_wait(empty(stage), phase ^ 1u, abort_flag, a.timeout_ns)) break;
+            const uint32_t nb = static_cast<uint32_t>(b / a.KB);
+            const uint32_t kb = static_cast<uint32_t>(b - static_cast<uint64_t>(nb) * a.KB);
+            if (elect_one()) {
+                mbar_arrive_expect_tx(full(stage), kWStageBytes);
+                tma_load_2d(sbase + stage * kWStageBytes, &tmW, full(stage), kb * 128, nb * 128);
+            }
+            __syncwarp();
+            ++issued;
+            if (++stage == kWStages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        for (int s = 0; s < kWStages; ++s) {
+            if (static_cast<uint32_t>(s) >= issued) break;
+            const uint32_t last = s + kWStages * ((issued - 1 - s) / kWStages);
+            volatile int local_flag = 0;
+            mbar_wait(full(s), (last / kWStages) & 1u, &local_flag, a.timeout_ns);
+        }
     } else {
         const int cw = warp - 1;
         const int grp = cw / kWGroupWarps, gw = cw % kWGroupWarps;
@@ -430,55 +390,13 @@ __global__ void __launch_bounds__(kWThreads, 1)
             const float r = fast ? __frcp_rn(sc) : 0.0f;
             const int64_t k = static_cast<int64_t>(kb) * 128 + 8 * (tid & 15u);
             const int64_t n0 = static_cast<int64_t>(nb) * 128 + (tid >> 4);
-            // this group's code tile for this block (TRANS)
-            const uint32_t ct = code_base + (2 * grp + (iter & 1u)) * kWCodeTile;
 #pragma unroll
             for (int j = 0; j < kWChunksPerThread; ++j) {
                 const int64_t n = n0 + (kStride / 16) * j;
-                const uint2 code = encode8_r(v[j], sc, r, fast);
-                if (a.q != nullptr && n < a.N && k < a.K)
-                    *reinterpret_cast<uint2*>(a.q + n * a.K + k) = code;
-                if constexpr (TRANS) {
-                    // tile row (tid >> 4) + 16 j, bytes 8 (tid & 15) .. + 7
-                    const uint32_t off = 128u * ((tid >> 4) + (kStride / 16) * j) + 8u * (tid & 15u);
-                    asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(ct + off), "r"(code.x),
-                                 "r"(code.y)
-                                 : "memory");
-                }
+                if (n < a.N && k < a.K)
+                    *reinterpret_cast<uint2*>(a.q + n * a.K + k) = encode8_r(v[j], sc, r, fast);
             }
-            if (tid == 0) {
-                if (a.s != nullptr) a.s[b] = sc;
-                if constexpr (TRANS) a.st[static_cast<uint64_t>(kb) * a.NB + nb] = sc;
-            }
-            if constexpr (TRANS) {
-                // All of the group's codes are in the tile once every warp has
-                // arrived; the tile used two blocks ago is free, because every
-                // warp passed this block's amax exchange after its last read.
-                __syncwarp();
-                if (lane == 0) mbar_arrive(codes_bar(grp));
-                if (!warp_wait(codes_bar(grp), iter & 1u, abort_flag, a.timeout_ns)) break;
-                const int64_t nrow = static_cast<int64_t>(nb) * 128 + 16 * gw;  // first n of the warp
-                uint32_t cols[4][4];  // [row quad][k byte i] -> 4 codes of n = nrow + 4 quad ..
-#pragma unroll
-                for (int qd = 0; qd < 4; ++qd) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int rr = 0; rr < 4; ++rr) {
-                        const uint32_t addr = ct + 128u * (16 * gw + 4 * qd + rr) + 4u * lane;
-                        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w[rr]) : "r"(addr));
-                    }
-                    transpose4x4(w, cols[qd]);
-                }
-                if (nrow < a.N) {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int64_t kk = static_cast<int64_t>(kb) * 128 + 4 * lane + i;
-                        if (kk < a.K)
-                            *reinterpret_cast<uint4*>(a.qt + kk * a.N + nrow) =
-                                make_uint4(cols[0][i], cols[1][i], cols[2][i], cols[3][i]);
-                    }
-                }
-            }
+            if (tid == 0) a.s[b] = sc;
             stage += kWGroups;
             if (stage >= kWStages) {
                 stage -= kWStages;
@@ -491,154 +409,300 @@ __global__ void __launch_bounds__(kWThreads, 1)
 }
 
 // ------------------------------------------------- activations, transposed
-// 128x1 tiles (one column, 128 consecutive rows): block (mb, kb) of x [M, K]
-// is one 128x128 TMA box holding 128 tiles, one per column. In a group, lane
-// l of warp w takes the column pair p = l + 32 (w & 1) (columns 2p, 2p + 1)
-// over the rows [32 (w >> 1), +32): one 4-byte word per row, so each
-// warp-wide load reads 32 consecutive words of one row. The four row
-// segments' column maxima meet in shared memory; each thread then encodes
-// its 2 x 32 values and writes 32 bytes into each of two rows of qt.
+// 128x1 tiles (one column, 128 consecutive rows), codes written transposed.
+// A CTA of 256 threads handles 128x128 blocks b = blockIdx.x, + gridDim.x,
+// ...; block b is (mb, kb) = (b % MB, b / MB), so the CTAs running at the
+// same time cover consecutive 128-row blocks of the same columns and their
+// writes to qt form long runs. In a block, warp w holds rows [16 w, 16 w +
+// 16) and lane l columns [4 l, 4 l + 4), read with 8-byte loads (a warp reads
+// 256 contiguous bytes of a row). The loads of the CTA's next block are
+// issued before the current block is encoded, so two blocks per CTA are in
+// flight. Column maxima meet in shared memory, one thread per column forms
+// the column's scale and reciprocal, and each thread then encodes its 16 x 4
+// values and writes one 16-byte run of qt per column.
+constexpr int kTThreads = 256;
+
 struct ActTArgs {
-    uint8_t* qt;  // [K, M]
-    float* st;    // [K, MB]
+    const uint8_t* x;  // bf16 [M, K]
+    uint8_t* qt;       // [K, M]
+    float* st;         // [K, MB]
     int64_t M, K;
     uint32_t MB, KB;
-    uint64_t timeout_ns;
 };
 
-constexpr int kTRedWords = 2 * 4 * 64;  // per group: [parity][row segment][column pair]
-constexpr int kTMiscBytes = 8 * kWBars + 16 + kWGroups * kTRedWords * 4;
-constexpr int kTSmem = kWStages * kWStageBytes + kTMiscBytes + 1024;
-
-// 32 values of one tile column (bf16 in the low or high half of w[r]) with
-// scale s and reciprocal r (0: the IEEE-divide range) -> 32 codes, row order.
-template <bool HI>
-__device__ __forceinline__ float col_value(uint32_t v) {
-    return __uint_as_float(HI ? (v & 0xFFFF0000u) : (v << 16));
+// Two quotients at once on packed pairs: (y0, y1) = (x0 / s0, x1 / s1) by
+// the steps of div_by_scale (q0 = RN(x r), e = RN(q0 s - x) exact,
+// q = RN(q0 - e r)), written with nx = -x and nr = -r so that every step is
+// a plain packed multiply or FMA; bit-identical to div_by_scale per lane.
+__device__ __forceinline__ void div2_by_scale(float x0, float x1, float nx0, float nx1, float s0,
+                                              float s1, float r0, float r1, float nr0, float nr1,
+                                              float& y0, float& y1) {
+    asm("{\n\t.reg .b64 x, nx, s, r, nr, q, e;\n\t"
+        "mov.b64 x, {%2, %3};\n\t"
+        "mov.b64 nx, {%4, %5};\n\t"
+        "mov.b64 s, {%6, %7};\n\t"
+        "mov.b64 r, {%8, %9};\n\t"
+        "mov.b64 nr, {%10, %11};\n\t"
+        "mul.rn.f32x2 q, x, r;\n\t"
+        "fma.rn.f32x2 e, q, s, nx;\n\t"
+        "fma.rn.f32x2 q, e, nr, q;\n\t"
+        "mov.b64 {%0, %1}, q;\n\t}"
+        : "=f"(y0), "=f"(y1)
+        : "f"(x0), "f"(x1), "f"(nx0), "f"(nx1), "f"(s0), "f"(s1), "f"(r0), "f"(r1), "f"(nr0),
+          "f"(nr1));
 }
 
-template <bool HI>
-__device__ __forceinline__ void encode_col32(const uint32_t (&w)[32], float s, float r, bool fast,
-                                             uint32_t (&out)[8]) {
-    if (s == 0.0f) {
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+// the same, negated (the sign bit flipped)
+__device__ __forceinline__ float bf16_lo_neg(uint32_t w) { return __uint_as_float(w * 65536u + 0x80000000u); }
+__device__ __forceinline__ float bf16_hi_neg(uint32_t w) { return __uint_as_float((w & 0xFFFF0000u) ^ 0x80000000u); }
+
+// Four columns x four rows: y[i][c] = x[row i][column c] / s_c, rows from
+// the words v[i] (columns 0, 1 in .x, 2, 3 in .y), then the codes of each
+// column's four rows packed low row first.
+template <bool FAST>
+__device__ __forceinline__ void encode_quad(const uint2 (&v)[4], const float4& s, const float4& r,
+                                            const float4& nr, uint32_t (&code)[4]) {
+    float y[4][4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) out[i] = 0u;
-    } else if (fast) {  // one branch per column, not per element
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float y0 = div_by_scale(col_value<HI>(w[4 * i]), s, r);
-            const float y1 = div_by_scale(col_value<HI>(w[4 * i + 1]), s, r);
-            const float y2 = div_by_scale(col_value<HI>(w[4 * i + 2]), s, r);
-            const float y3 = div_by_scale(col_value<HI>(w[4 * i + 3]), s, r);
-            out[i] = e4m3x2(y0, y1) | (e4m3x2(y2, y3) << 16);
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t a = v[i].x, b = v[i].y;
+        if constexpr (FAST) {
+            div2_by_scale(bf16_lo(a), bf16_hi(a), bf16_lo_neg(a), bf16_hi_neg(a), s.x, s.y, r.x, r.y,
+                          nr.x, nr.y, y[i][0], y[i][1]);
+            div2_by_scale(bf16_lo(b), bf16_hi(b), bf16_lo_neg(b), bf16_hi_neg(b), s.z, s.w, r.z, r.w,
+                          nr.z, nr.w, y[i][2], y[i][3]);
+        } else {
+            y[i][0] = __fdiv_rn(bf16_lo(a), s.x);
+            y[i][1] = __fdiv_rn(bf16_hi(a), s.y);
+            y[i][2] = __fdiv_rn(bf16_lo(b), s.z);
+            y[i][3] = __fdiv_rn(bf16_hi(b), s.w);
         }
-    } else {
+    }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float y0 = __fdiv_rn(col_value<HI>(w[4 * i]), s);
-            const float y1 = __fdiv_rn(col_value<HI>(w[4 * i + 1]), s);
-            const float y2 = __fdiv_rn(col_value<HI>(w[4 * i + 2]), s);
-            const float y3 = __fdiv_rn(col_value<HI>(w[4 * i + 3]), s);
-            out[i] = e4m3x2(y0, y1) | (e4m3x2(y2, y3) << 16);
+    for (int c = 0; c < 4; ++c) code[c] = e4m3x2(y[0][c], y[1][c]) | (e4m3x2(y[2][c], y[3][c]) << 16);
+}
+
+__device__ __forceinline__ void load_block_t(const ActTArgs& a, uint32_t b, int w, int l,
+                                             uint2 (&v)[16]) {
+    const uint32_t mb = b % a.MB, kb = b / a.MB;
+    const int64_t k = static_cast<int64_t>(kb) * 128 + 4 * l;
+    const int64_t m0 = static_cast<int64_t>(mb) * 128 + 16 * w;
+    const bool live = k < a.K && m0 < a.M;  // K % 4 == 0 and M % 16 == 0: all or nothing
+    const uint2* src = reinterpret_cast<const uint2*>(a.x + 2 * (live ? m0 * a.K + k : 0));
+    const int64_t pitch = a.K / 4;  // uint2 per row
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = live ? __ldg(src + i * pitch) : make_uint2(0u, 0u);
+}
+
+__global__ void __launch_bounds__(kTThreads, 2) quant_act_t_kernel(const ActTArgs a) {
+    __shared__ uint32_t red[8][64];  // [warp][column pair]: packed |bf16| maxima
+    __shared__ float4 s_sh[32], r_sh[32];
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    const uint32_t nblocks = a.MB * a.KB;
+    uint2 v[16];
+    if (blockIdx.x < nblocks) load_block_t(a, blockIdx.x, w, l, v);
+    for (uint32_t b = blockIdx.x; b < nblocks; b += gridDim.x) {
+        uint2 vn[16];
+        if (b + gridDim.x < nblocks) load_block_t(a, b + gridDim.x, w, l, vn);
+        const uint32_t mb = b % a.MB, kb = b / a.MB;
+        const int64_t k = static_cast<int64_t>(kb) * 128 + 4 * l;
+        const int64_t m0 = static_cast<int64_t>(mb) * 128 + 16 * w;
+        const bool live = k < a.K && m0 < a.M;
+        uint32_t mx0 = 0, mx1 = 0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            mx0 = __vmaxu2(mx0, v[i].x & 0x7FFF7FFFu);
+            mx1 = __vmaxu2(mx1, v[i].y & 0x7FFF7FFFu);
         }
+        red[w][2 * l] = mx0;
+        red[w][2 * l + 1] = mx1;
+        __syncthreads();
+        if (threadIdx.x < 128) {
+            const int c = threadIdx.x;  // column of the block
+            uint32_t m = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) m = __vmaxu2(m, red[i][c >> 1]);
+            const float amax = __uint_as_float((c & 1) ? (m & 0xFFFF0000u) : (m << 16));
+            const float sc = tile_scale(amax);
+            const float rc = amax >= kFastDivMinAmax ? __frcp_rn(sc) : 0.0f;
+            reinterpret_cast<float*>(s_sh)[c] = sc;
+            reinterpret_cast<float*>(r_sh)[c] = rc;
+            const int64_t col = static_cast<int64_t>(kb) * 128 + c;
+            if (col < a.K) a.st[col * a.MB + mb] = sc;
+        }
+        __syncthreads();
+        if (live) {
+            const float4 s = s_sh[l], r = r_sh[l];
+            const float4 nr = make_float4(-r.x, -r.y, -r.z, -r.w);
+            // every column either all-zero (s = 0, masked below) or in the fast range
+            const bool fast = (s.x == 0.0f || r.x != 0.0f) && (s.y == 0.0f || r.y != 0.0f) &&
+                              (s.z == 0.0f || r.z != 0.0f) && (s.w == 0.0f || r.w != 0.0f);
+            uint32_t code[4][4];  // [column][row quad]
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint2 vq[4] = {v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]};
+                uint32_t cq[4];
+                if (fast) encode_quad<true>(vq, s, r, nr, cq);
+                else encode_quad<false>(vq, s, r, nr, cq);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) code[c][q] = cq[c];
+            }
+            const float sv[4] = {s.x, s.y, s.z, s.w};
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const uint4 out = sv[c] == 0.0f
+                                      ? make_uint4(0u, 0u, 0u, 0u)
+                                      : make_uint4(code[c][0], code[c][1], code[c][2], code[c][3]);
+                *reinterpret_cast<uint4*>(a.qt + (k + c) * a.M + m0) = out;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = vn[i];
     }
 }
 
-__global__ void __launch_bounds__(kWThreads, 1)
-    quant_act_t_kernel(const __grid_constant__ CUtensorMap tmX, const ActTArgs a) {
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
-    const uint32_t sbase = raw + pad;
-    const uint32_t bar_base = sbase + kWStages * kWStageBytes;
-    auto full = [&](int s) { return bar_base + 8u * s; };
-    auto empty = [&](int s) { return bar_base + 8u * (kWStages + s); };
-    auto red_bar = [&](int g) { return bar_base + 8u * (2 * kWStages + g); };
-    uint8_t* misc = smem_raw + pad + kWStages * kWStageBytes + 8 * kWBars;
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(misc);
-    uint32_t* red = reinterpret_cast<uint32_t*>(misc + 16);  // [groups][kTRedWords]
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint64_t nblocks = static_cast<uint64_t>(a.MB) * a.KB;
+// Four 4-byte words (rows r0..r3 of a byte matrix, column bytes 0..3) ->
+// four words holding its columns: out[i] byte j = in[j] byte i.
+__device__ __forceinline__ void transpose4x4(const uint32_t (&in)[4], uint32_t (&out)[4]) {
+    const uint32_t t0 = __byte_perm(in[0], in[1], 0x5140);  // r0b0 r1b0 r0b1 r1b1
+    const uint32_t t1 = __byte_perm(in[0], in[1], 0x7362);  // r0b2 r1b2 r0b3 r1b3
+    const uint32_t t2 = __byte_perm(in[2], in[3], 0x5140);
+    const uint32_t t3 = __byte_perm(in[2], in[3], 0x7362);
+    out[0] = __byte_perm(t0, t2, 0x5410);
+    out[1] = __byte_perm(t0, t2, 0x7632);
+    out[2] = __byte_perm(t1, t3, 0x5410);
+    out[3] = __byte_perm(t1, t3, 0x7632);
+}
 
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < kWStages; ++s) {
-            mbar_init(full(s), 1);
-            mbar_init(empty(s), kWGroupWarps);
-        }
-        for (int g = 0; g < kWGroups; ++g) mbar_init(red_bar(g), kWGroupWarps);
-        *abort_flag = 0;
-        fence_barrier_init();
-        fence_proxy_async_smem();
-    }
-    if (warp == 0 && lane == 0) prefetch_tmap(&tmX);
-    __syncthreads();
+// ------------------------------------------------- weights, plain blocks
+// 128x128 blocks with one scale each, the same thread layout as the
+// transposed activation kernel (warp w: rows [16 w, +16); lane l: columns
+// [4 l, +4); the next block's loads in flight while the current one is
+// encoded). WQ writes the codes row-major (q [N, K], 4 bytes per row per
+// lane: a warp writes 128 contiguous bytes of each row), WT transposed
+// (qt [K, N], one 16-byte run per column per lane). Blocks are taken with
+// the 128-row blocks fastest when WT is set (runs along qt rows), else the
+// 128-column blocks fastest (runs along q rows).
+struct WeightPlainArgs {
+    const uint8_t* w;  // bf16 [N, K]
+    uint8_t* q;        // [N, K] (WQ)
+    float* s;          // [NB, KB] (WQ)
+    uint8_t* qt;       // [K, N] (WT)
+    float* st;         // [KB, NB] (WT)
+    int64_t N, K;
+    uint32_t NB, KB;
+};
 
-    if (warp == 0) {
-        block_producer(&tmX, nblocks, a.KB, sbase, bar_base, abort_flag, a.timeout_ns);
+template <bool WT>
+__device__ __forceinline__ void weight_block_coords(const WeightPlainArgs& a, uint32_t b, uint32_t& nb,
+                                                    uint32_t& kb) {
+    if constexpr (WT) {
+        nb = b % a.NB;
+        kb = b / a.NB;
     } else {
-        const int cw = warp - 1;
-        const int grp = cw / kWGroupWarps, gw = cw % kWGroupWarps;
-        const uint32_t pr = static_cast<uint32_t>(lane) + 32u * (gw & 1);  // column pair
-        const uint32_t seg = static_cast<uint32_t>(gw >> 1);               // row segment
-        uint32_t* red_g = red + grp * kTRedWords;
-        int stage = grp;
-        uint32_t phase = 0, iter = 0;
-        for (uint64_t b = blockIdx.x + static_cast<uint64_t>(grp) * gridDim.x; b < nblocks;
-             b += static_cast<uint64_t>(kWGroups) * gridDim.x, ++iter) {
-            if (!warp_wait(full(stage), phase, abort_flag, a.timeout_ns)) break;
-            const uint32_t mb = static_cast<uint32_t>(b / a.KB);
-            const uint32_t kb = static_cast<uint32_t>(b - static_cast<uint64_t>(mb) * a.KB);
-            const uint32_t st = sbase + stage * kWStageBytes + 256u * 32u * seg + 4u * pr;
-            uint32_t w[32];
+        kb = b % a.KB;
+        nb = b / a.KB;
+    }
+}
+
+template <bool WT>
+__device__ __forceinline__ void load_weight_block(const WeightPlainArgs& a, uint32_t b, int w, int l,
+                                                  uint2 (&v)[16]) {
+    uint32_t nb, kb;
+    weight_block_coords<WT>(a, b, nb, kb);
+    const int64_t k = static_cast<int64_t>(kb) * 128 + 4 * l;
+    const int64_t n0 = static_cast<int64_t>(nb) * 128 + 16 * w;
+    const uint2* src = reinterpret_cast<const uint2*>(a.w + 2 * (k < a.K ? n0 * a.K + k : 0));
+    const int64_t pitch = a.K / 4;
 #pragma unroll
-            for (int r = 0; r < 32; ++r)
-                asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w[r]) : "r"(st + 256u * r));
-            __syncwarp();
-            if (lane == 0) mbar_arrive(empty(stage));
-            uint32_t mx = 0;
+    for (int i = 0; i < 16; ++i)
+        v[i] = (k < a.K && n0 + i < a.N) ? __ldg(src + i * pitch) : make_uint2(0u, 0u);
+}
+
+template <bool WQ, bool WT>
+__global__ void __launch_bounds__(kTThreads, 2) quant_weight_plain_kernel(const WeightPlainArgs a) {
+    __shared__ uint32_t red[8];
+    __shared__ float2 sr_sh;  // the block's scale and reciprocal (0: IEEE-divide range)
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    const uint32_t nblocks = a.NB * a.KB;
+    uint2 v[16];
+    if (blockIdx.x < nblocks) load_weight_block<WT>(a, blockIdx.x, w, l, v);
+    for (uint32_t b = blockIdx.x; b < nblocks; b += gridDim.x) {
+        uint2 vn[16];
+        if (b + gridDim.x < nblocks) load_weight_block<WT>(a, b + gridDim.x, w, l, vn);
+        uint32_t nb, kb;
+        weight_block_coords<WT>(a, b, nb, kb);
+        const int64_t k = static_cast<int64_t>(kb) * 128 + 4 * l;
+        const int64_t n0 = static_cast<int64_t>(nb) * 128 + 16 * w;
+        uint32_t mx = 0;
 #pragma unroll
-            for (int r = 0; r < 32; ++r) mx = __vmaxu2(mx, w[r] & 0x7FFF7FFFu);
-            // column maxima across the four row segments (halves of red_g
-            // alternate per block, as in the weight kernel's exchange)
-            uint32_t* rb = red_g + (iter & 1u) * (kTRedWords / 2);
-            rb[64 * seg + pr] = mx;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(red_bar(grp));
-            if (!warp_wait(red_bar(grp), iter & 1u, abort_flag, a.timeout_ns)) break;
-            const uint32_t m2 = __vmaxu2(__vmaxu2(rb[pr], rb[64 + pr]), __vmaxu2(rb[128 + pr], rb[192 + pr]));
-            const float amax0 = __uint_as_float(m2 << 16), amax1 = __uint_as_float(m2 & 0xFFFF0000u);
-            const float s0 = tile_scale(amax0), s1 = tile_scale(amax1);
-            const bool fast0 = amax0 >= kFastDivMinAmax, fast1 = amax1 >= kFastDivMinAmax;
-            const float r0 = fast0 ? __frcp_rn(s0) : 0.0f, r1 = fast1 ? __frcp_rn(s1) : 0.0f;
-            uint32_t c0[8], c1[8];
-            encode_col32<false>(w, s0, r0, fast0, c0);
-            encode_col32<true>(w, s1, r1, fast1, c1);
-            const int64_t k = static_cast<int64_t>(kb) * 128 + 2 * pr;
-            const int64_t m0 = static_cast<int64_t>(mb) * 128 + 32 * seg;
+        for (int i = 0; i < 16; ++i) mx = __vmaxu2(mx, __vmaxu2(v[i].x & 0x7FFF7FFFu, v[i].y & 0x7FFF7FFFu));
+        mx = max(mx & 0xFFFFu, mx >> 16);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {  // 16 rows each (M % 16 == 0)
-                if (m0 + 16 * h < a.M) {
-                    if (k < a.K)
-                        *reinterpret_cast<uint4*>(a.qt + k * a.M + m0 + 16 * h) =
-                            make_uint4(c0[4 * h], c0[4 * h + 1], c0[4 * h + 2], c0[4 * h + 3]);
-                    if (k + 1 < a.K)
-                        *reinterpret_cast<uint4*>(a.qt + (k + 1) * a.M + m0 + 16 * h) =
-                            make_uint4(c1[4 * h], c1[4 * h + 1], c1[4 * h + 2], c1[4 * h + 3]);
+        for (int d = 16; d >= 1; d >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, d));
+        if (l == 0) red[w] = mx;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            uint32_t m = red[0];
+#pragma unroll
+            for (int i = 1; i < 8; ++i) m = max(m, red[i]);
+            const float amax = __uint_as_float(m << 16);
+            const float sc = tile_scale(amax);
+            sr_sh = make_float2(sc, amax >= kFastDivMinAmax ? __frcp_rn(sc) : 0.0f);
+            if constexpr (WQ) a.s[static_cast<uint64_t>(nb) * a.KB + kb] = sc;
+            if constexpr (WT) a.st[static_cast<uint64_t>(kb) * a.NB + nb] = sc;
+        }
+        __syncthreads();
+        const float2 sr = sr_sh;
+        if (k < a.K && sr.x != 0.0f) {
+            const float4 s4 = make_float4(sr.x, sr.x, sr.x, sr.x);
+            const float4 r4 = make_float4(sr.y, sr.y, sr.y, sr.y);
+            const float4 nr4 = make_float4(-sr.y, -sr.y, -sr.y, -sr.y);
+            uint32_t colc[4][4];  // [column][row quad]
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint2 vq[4] = {v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]};
+                uint32_t cq[4];
+                if (sr.y != 0.0f) encode_quad<true>(vq, s4, r4, nr4, cq);
+                else encode_quad<false>(vq, s4, r4, nr4, cq);
+                if constexpr (WQ) {
+                    uint32_t rows[4];  // row i: the codes of columns k .. k + 3
+                    transpose4x4(cq, rows);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        if (n0 + 4 * q + i < a.N)
+                            *reinterpret_cast<uint32_t*>(a.q + (n0 + 4 * q + i) * a.K + k) = rows[i];
+                }
+#pragma unroll
+                for (int c = 0; c < 4; ++c) colc[c][q] = cq[c];
+            }
+            if constexpr (WT) {
+                if (n0 < a.N) {  // N % 16 == 0: the 16 rows are all present
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        *reinterpret_cast<uint4*>(a.qt + (k + c) * a.N + n0) =
+                            make_uint4(colc[c][0], colc[c][1], colc[c][2], colc[c][3]);
                 }
             }
-            if (seg == 0) {
-                if (k < a.K) a.st[k * a.MB + mb] = s0;
-                if (k + 1 < a.K) a.st[(k + 1) * a.MB + mb] = s1;
+        } else if (k < a.K) {  // all-zero block: codes 0
+            if constexpr (WQ) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    if (n0 + i < a.N) *reinterpret_cast<uint32_t*>(a.q + (n0 + i) * a.K + k) = 0u;
             }
-            stage += kWGroups;
-            if (stage >= kWStages) {
-                stage -= kWStages;
-                phase ^= 1u;
+            if constexpr (WT) {
+                if (n0 < a.N) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        *reinterpret_cast<uint4*>(a.qt + (k + c) * a.N + n0) = make_uint4(0u, 0u, 0u, 0u);
+                }
             }
         }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = vn[i];
     }
-    __syncthreads();
-    if (threadIdx.x == 0 && *abort_flag) atomicOr(&g_quant_status, FP8Q_DEVSTATUS_TIMEOUT);
 }
 
 // ------------------------------------------------------------------ gather
@@ -679,7 +743,6 @@ __global__ void __launch_bounds__(kGatherThreads) gather_rows_kernel(
 }
 
 }  // namespace
-
 cudaError_t launch_gather_rows(const void* q_src, const float* s_src, int64_t T, int64_t K,
                                const int32_t* index, int64_t R, void* q_dst, float* s_dst,
                                cudaStream_t stream, int num_sms) {
@@ -719,14 +782,11 @@ cudaError_t launch_quant_act(const void* x, int64_t M, int64_t K, void* q, float
     return cudaGetLastError();
 }
 
-cudaError_t launch_quant_weight(const CUtensorMap* tmW, void* q, float* s, void* qt, float* st,
-                                int64_t N, int64_t K, cudaStream_t stream, int num_sms,
-                                uint64_t timeout_ns) {
+cudaError_t launch_quant_weight(const CUtensorMap* tmW, void* q, float* s, int64_t N, int64_t K,
+                                cudaStream_t stream, int num_sms, uint64_t timeout_ns) {
     WeightArgs a;
     a.q = static_cast<uint8_t*>(q);
     a.s = s;
-    a.qt = static_cast<uint8_t*>(qt);
-    a.st = st;
     a.N = N;
     a.K = K;
     a.NB = static_cast<uint32_t>((N + 127) / 128);
@@ -734,36 +794,59 @@ cudaError_t launch_quant_weight(const CUtensorMap* tmW, void* q, float* s, void*
     a.timeout_ns = timeout_ns;
     const uint64_t nblocks = static_cast<uint64_t>(a.NB) * a.KB;
     const unsigned grid = static_cast<unsigned>(nblocks < static_cast<uint64_t>(num_sms) ? nblocks : num_sms);
-    if (qt != nullptr) {
-        cudaError_t err = cudaFuncSetAttribute(quant_weight_kernel<true>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, kWSmemT);
-        if (err != cudaSuccess) return err;
-        quant_weight_kernel<true><<<grid, kWThreads, kWSmemT, stream>>>(*tmW, a);
-    } else {
-        cudaError_t err = cudaFuncSetAttribute(quant_weight_kernel<false>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, kWSmem);
-        if (err != cudaSuccess) return err;
-        quant_weight_kernel<false><<<grid, kWThreads, kWSmem, stream>>>(*tmW, a);
-    }
+    cudaError_t err =
+        cudaFuncSetAttribute(quant_weight_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kWSmem);
+    if (err != cudaSuccess) return err;
+    quant_weight_kernel<<<grid, kWThreads, kWSmem, stream>>>(*tmW, a);
     return cudaGetLastError();
 }
 
-cudaError_t launch_quant_act_t(const CUtensorMap* tmX, void* qt, float* st, int64_t M, int64_t K,
-                               cudaStream_t stream, int num_sms, uint64_t timeout_ns) {
+template <bool WQ, bool WT>
+cudaError_t launch_weight_plain(const WeightPlainArgs& a, cudaStream_t stream, int num_sms) {
+    int per_sm = 0;
+    cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &per_sm, quant_weight_plain_kernel<WQ, WT>, kTThreads, 0);
+    if (err != cudaSuccess) return err;
+    const uint64_t nblocks = static_cast<uint64_t>(a.NB) * a.KB;
+    const uint64_t cap = static_cast<uint64_t>(num_sms) * (per_sm > 0 ? per_sm : 1);
+    quant_weight_plain_kernel<WQ, WT>
+        <<<static_cast<unsigned>(nblocks < cap ? nblocks : cap), kTThreads, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_weight_t(const void* w, void* q, float* s, void* qt, float* st, int64_t N,
+                                  int64_t K, cudaStream_t stream, int num_sms) {
+    WeightPlainArgs p;
+    p.w = static_cast<const uint8_t*>(w);
+    p.q = static_cast<uint8_t*>(q);
+    p.s = s;
+    p.qt = static_cast<uint8_t*>(qt);
+    p.st = st;
+    p.N = N;
+    p.K = K;
+    p.NB = static_cast<uint32_t>((N + 127) / 128);
+    p.KB = static_cast<uint32_t>((K + 127) / 128);
+    if (q == nullptr) return launch_weight_plain<false, true>(p, stream, num_sms);
+    return launch_weight_plain<true, true>(p, stream, num_sms);
+}
+
+cudaError_t launch_quant_act_t(const void* x, void* qt, float* st, int64_t M, int64_t K,
+                               cudaStream_t stream, int num_sms) {
     ActTArgs a;
+    a.x = static_cast<const uint8_t*>(x);
     a.qt = static_cast<uint8_t*>(qt);
     a.st = st;
     a.M = M;
     a.K = K;
     a.MB = static_cast<uint32_t>((M + 127) / 128);
     a.KB = static_cast<uint32_t>((K + 127) / 128);
-    a.timeout_ns = timeout_ns;
-    const uint64_t nblocks = static_cast<uint64_t>(a.MB) * a.KB;
-    const unsigned grid = static_cast<unsigned>(nblocks < static_cast<uint64_t>(num_sms) ? nblocks : num_sms);
-    cudaError_t err =
-        cudaFuncSetAttribute(quant_act_t_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTSmem);
+    int per_sm = 0;
+    cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quant_act_t_kernel,
+                                                                    kTThreads, 0);
     if (err != cudaSuccess) return err;
-    quant_act_t_kernel<<<grid, kWThreads, kTSmem, stream>>>(*tmX, a);
+    const uint64_t nblocks = static_cast<uint64_t>(a.MB) * a.KB;
+    const uint64_t cap = static_cast<uint64_t>(num_sms) * (per_sm > 0 ? per_sm : 1);
+    quant_act_t_kernel<<<static_cast<unsigned>(nblocks < cap ? nblocks : cap), kTThreads, 0, stream>>>(a);
     return cudaGetLastError();
 }
 

@@ -9,15 +9,17 @@ namespace fp8q {
 
 cudaError_t launch_quant_act(const void* x, int64_t M, int64_t K, void* q, float* s,
                              cudaStream_t stream, int num_sms, uint64_t timeout_ns);
-// tmW: bf16 [N, K] tensor map, box 128 x 128, no swizzle. q and s may be
-// null when qt is not; qt/st (the transposed layout) may be null.
-cudaError_t launch_quant_weight(const CUtensorMap* tmW, void* q, float* s, void* qt, float* st,
-                                int64_t N, int64_t K, cudaStream_t stream, int num_sms,
-                                uint64_t timeout_ns);
-// tmX: bf16 [M, K] tensor map, box 128 x 128, no swizzle; 128x1 tiles,
-// codes written transposed [K, M], scales [K, ceil(M/128)]
-cudaError_t launch_quant_act_t(const CUtensorMap* tmX, void* qt, float* st, int64_t M, int64_t K,
-                               cudaStream_t stream, int num_sms, uint64_t timeout_ns);
+// tmW: bf16 [N, K] tensor map, box 128 x 128, no swizzle
+cudaError_t launch_quant_weight(const CUtensorMap* tmW, void* q, float* s, int64_t N, int64_t K,
+                                cudaStream_t stream, int num_sms, uint64_t timeout_ns);
+// w: bf16 [N, K] (N % 16 == 0, K % 16 == 0); writes qt [K, N] and st
+// [KB, NB], and q [N, K] and s [NB, KB] unless q is null
+cudaError_t launch_quant_weight_t(const void* w, void* q, float* s, void* qt, float* st, int64_t N,
+                                  int64_t K, cudaStream_t stream, int num_sms);
+// x: bf16 [M, K] (M % 16 == 0, K % 16 == 0); 128x1 tiles, codes written
+// transposed [K, M], scales [K, ceil(M/128)]
+cudaError_t launch_quant_act_t(const void* x, void* qt, float* st, int64_t M, int64_t K,
+                               cudaStream_t stream, int num_sms);
 cudaError_t launch_gather_rows(const void* q_src, const float* s_src, int64_t T, int64_t K,
                                const int32_t* index, int64_t R, void* q_dst, float* s_dst,
                                cudaStream_t stream, int num_sms);
