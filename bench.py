@@ -208,6 +208,8 @@ class Path:
         self.names = (["quant_act"] + [f"quant_weight[{n}]" for n in w.weights]
                       + [f"gemm[{n}]" for n in w.weights])
         self.gemm_names = [f"gemm[{n}]" for n in w.weights]
+        self.dominant = self.gemm_names  # the roofline kernel(s)
+        self.dominant_flops = self.flops
         self.describe = (w.name + ": quant_act(A) + quant_weight(W) + "
                          + ("grouped" if w.offsets is not None else "dense")
                          + " block-scaled GEMM per step")
@@ -304,6 +306,8 @@ class BackwardPath:
         self.names = ["quant_act[dY]", "quant_weight_t[W]", "gemm[dX]", "quant_act_t[dY]",
                       "quant_act_t[X]", "gemm[dW]"]
         self.gemm_names = ["gemm[dX]", "gemm[dW]"]
+        self.dominant = ["gemm[dW]"]  # the largest share of the step
+        self.dominant_flops = 2.0 * T * N * K
         self.describe = (w.name + ": quant_act(dY) + quant_weight_t(W) + dX GEMM + "
                          "quant_act_t(dY) + quant_act_t(X) + dW GEMM per step")
 
@@ -528,30 +532,41 @@ def main():
         if "GB/s" in v:
             v["frac_hbm"] = v["GB/s"] / peaks["hbm_gbs"]
 
-    # dominant kernel: the GEMM(s). It runs inside a long back-to-back loop
-    # (power-capped), so the sustained measured figure is its denominator;
-    # the burst-based fraction is reported beside it.
+    # dominant kernel: the GEMM(s) (the weight-gradient GEMM in the backward
+    # step). It runs inside a long back-to-back loop (power-capped), so the
+    # sustained measured figure is its denominator; the burst-based fraction
+    # is reported beside it.
     t_gemm = sum(per[n] for n in path.gemm_names)
+    t_dom = sum(per[n] for n in path.dominant)
     sustained = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
     fp8_peak = sustained * FP8_OVER_BF16
     fp8_burst = peaks["bf16_tflops"] * FP8_OVER_BF16
-    gemm_tflops = flops / t_gemm / 1e12
+    gemm_tflops = path.dominant_flops / t_dom / 1e12
     traffic = None
+    kernel_profiles = {}
     if args.config == 3:
         traffic = profiled_traffic("gemm_dense_8192x7168x7168.md", "gemm.cu")
-        for kname, prof in (("quant_act", "quant_act_8192x7168.md"),
-                            ("quant_weight[B]", "quant_weight_7168x7168.md")):
-            kern[kname]["traffic_bytes_per_launch"] = profiled_traffic(prof, "quant.cu")
+        kernel_profiles = {"quant_act": ("quant_act_8192x7168.md", "quant.cu"),
+                           "quant_weight[B]": ("quant_weight_7168x7168.md", "quant.cu")}
+    elif args.config == 8:
+        traffic = profiled_traffic("gemm_wgrad_7168x7168x8192.md", "gemm.cu")
+        kernel_profiles = {"quant_act[dY]": ("quant_act_8192x7168.md", "quant.cu"),
+                           "quant_weight_t[W]": ("quant_weight_t_7168x7168.md", "quant.cu"),
+                           "gemm[dX]": ("gemm_dense_8192x7168x7168.md", "gemm.cu"),
+                           "quant_act_t[dY]": ("quant_act_t_8192x7168.md", "quant.cu"),
+                           "quant_act_t[X]": ("quant_act_t_8192x7168.md", "quant.cu")}
+    for kname, (prof, src) in kernel_profiles.items():
+        kern[kname]["traffic_bytes_per_launch"] = profiled_traffic(prof, src)
     roofline = {"bound": "tensor", "achieved": gemm_tflops, "peak": fp8_peak, "unit": "TFLOP/s",
                 "frac": gemm_tflops / fp8_peak, "traffic": traffic,
                 "traffic_unit": "DRAM bytes per launch (ncu, profiles/)",
                 "frac_of_burst_peak": gemm_tflops / fp8_burst,
-                "kernel": "fp8_gemm_kernel", "peak_source":
+                "kernel": "fp8_gemm_kernel " + "+".join(path.dominant), "peak_source":
                     f"{peak_kind} bf16 sustained {sustained} TFLOP/s x {FP8_OVER_BF16} "
                     f"(nominal FP8:BF16 ratio); burst {peaks['bf16_tflops']} x {FP8_OVER_BF16} = "
                     f"{fp8_burst:.1f}"}
-    if len(path.gemm_names) > 1:
-        roofline["achieved_over"] = "+".join(path.gemm_names) + " (total GEMM FLOPs / total GEMM time)"
+    if len(path.dominant) > 1:
+        roofline["achieved_over"] = "+".join(path.dominant) + " (total GEMM FLOPs / total GEMM time)"
     if w.offsets is not None:
         # the grouped GEMM streams every expert's weights once: HBM-bound
         M = w.A.shape[0]
