@@ -233,8 +233,8 @@ FP8Q_API int fp8q_set_gemm_pairs(int enable);
 
 /*
  * Failure injection for tests of the device-side failure path. With
- * FP8Q_INJECT_STALLED_STAGE set, every fp8_block_gemm / fp8_grouped_gemm
- * launch announces 16 more bytes for its first pipeline stage than the
+ * FP8Q_INJECT_STALLED_STAGE set, every fp8_block_gemm / fp8_wgrad_gemm /
+ * fp8_grouped_gemm launch announces 16 more bytes for its first pipeline stage than the
  * stage receives, so that stage never completes: the kernel's bounded waits
  * expire (see fp8q_set_wait_timeout_ns), it drains its copies, frees its
  * tensor memory, writes nothing further, returns, and the device status word

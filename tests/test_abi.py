@@ -136,3 +136,57 @@ def test_gather_argument_checks(lib):
     assert _ga(lib, P, P, 8, 120, P, 4, P, P, None) == ALIGN
     assert _ga(lib, P + 8, P, 8, 128, P, 4, P, P, None) == ALIGN
     assert _ga(lib, P, P, 8, 128, P + 2, 4, P, P, None) == ALIGN
+
+
+def _qt(lib, *a):
+    f = lib.fp8q_quant_act_t
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+                  ctypes.c_void_p, ctypes.c_void_p]
+    return f(*a)
+
+
+def _wt(lib, *a):
+    f = lib.fp8q_quant_weight_t
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64] + [ctypes.c_void_p] * 5
+    return f(*a)
+
+
+def _wg(lib, *a):
+    f = lib.fp8_wgrad_gemm
+    f.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int64] * 3 + [ctypes.c_void_p]
+    return f(*a)
+
+
+def test_quant_act_t_argument_checks(lib):
+    assert _qt(lib, P, -1, 128, P, P, None) == SHAPE
+    assert _qt(lib, P, 16, 0, P, P, None) == SHAPE
+    assert _qt(lib, None, 0, 128, None, None, None) == OK
+    assert _qt(lib, None, 16, 128, P, P, None) == NULL
+    assert _qt(lib, P, 16, 128, None, P, None) == NULL
+    assert _qt(lib, P, 16, 128, P, None, None) == NULL
+    assert _qt(lib, P, 24, 128, P, P, None) == ALIGN   # M % 16: the row pitch of qt
+    assert _qt(lib, P, 16, 120, P, P, None) == ALIGN   # K % 16
+    assert _qt(lib, P, 16, 128, P + 8, P, None) == ALIGN
+
+
+def test_quant_weight_t_argument_checks(lib):
+    assert _wt(lib, P, -16, 128, P, P, P, P, None) == SHAPE
+    assert _wt(lib, None, 0, 128, None, None, None, None, None) == OK
+    assert _wt(lib, P, 16, 128, P, P, None, P, None) == NULL     # qt required
+    assert _wt(lib, P, 16, 128, P, P, P, None, None) == NULL     # st required
+    assert _wt(lib, P, 16, 128, P, None, P, P, None) == NULL     # q without s
+    assert _wt(lib, P, 16, 128, None, P, P, P, None) == NULL     # s without q
+    assert _wt(lib, P, 40, 128, None, None, P, P, None) == ALIGN  # N % 16
+    assert _wt(lib, P, 16, 120, None, None, P, P, None) == ALIGN  # K % 16
+    assert _wt(lib, P, 16, 128, P + 4, P, P, P, None) == ALIGN
+
+
+def test_wgrad_gemm_argument_checks(lib):
+    assert _wg(lib, P, P, P, P, P, -1, 256, 512, None) == SHAPE
+    assert _wg(lib, None, None, None, None, None, 0, 256, 512, None) == OK
+    for i in range(5):
+        args = [P] * 5
+        args[i] = None
+        assert _wg(lib, *args, 128, 256, 512, None) == NULL
+    assert _wg(lib, P, P, P, P, P, 128, 256, 520, None) == ALIGN
+    assert _wg(lib, P, P, P, P, P, 128, 252, 512, None) == ALIGN

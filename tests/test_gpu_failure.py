@@ -70,3 +70,28 @@ def test_grouped_stalled_stage_times_out(q):
     assert q.fp8q_get_device_status() == 0
     c32, S = oracle.grouped_gemm(qa, sa, qb, sb, off, rows=np.arange(300))
     assert_gemm_ok(to_f32(C), c32, S, "grouped GEMM after an injected timeout")
+
+
+@pytest.mark.parametrize("pairs", [True, False])
+def test_wgrad_stalled_stage_times_out(q, pairs):
+    # the row-scaled (weight-gradient) kernel shares the bounded waits; its
+    # scale ring holds a slot until the slot's last K block, so a stall
+    # there must unwind as well
+    q.fp8q_set_gemm_pairs(pairs)
+    rng = np.random.default_rng(5)
+    t = lambda a: torch.from_numpy(a).to(DEV)
+    M, N, K = 384, 256, 1024
+    qa = rng.choice(FINITE, size=(M, K)).astype(np.uint8)
+    qb = rng.choice(FINITE, size=(N, K)).astype(np.uint8)
+    sa = rng.uniform(0.01, 2, (M, K // 128)).astype(np.float32)
+    sb = rng.uniform(0.01, 2, (N, K // 128)).astype(np.float32)
+    q.fp8q_set_wait_timeout_ns(20_000_000)
+    q.fp8q_set_fault_injection(q.INJECT_STALLED_STAGE)
+    q.fp8_wgrad_gemm(t(qa), t(sa), t(qb), t(sb))
+    assert q.fp8q_get_device_status() & q.DEVSTATUS_TIMEOUT
+    q.fp8q_set_fault_injection(0)
+    q.fp8q_set_wait_timeout_ns(0)
+    C = q.fp8_wgrad_gemm(t(qa), t(sa), t(qb), t(sb))
+    assert q.fp8q_get_device_status() == 0
+    c32, S = oracle.wgrad_gemm(qa, sa, qb, sb)
+    assert_gemm_ok(to_f32(C), c32, S, "weight-gradient GEMM after an injected timeout")
