@@ -64,6 +64,8 @@ def _load():
         lib.fp8o_e4m3_encode_n.argtypes = [p, i64, p]
         lib.fp8o_quant_act.argtypes = [p, i64, i64, i64, i64, p, p]
         lib.fp8o_quant_weight.argtypes = [p, i64, i64, i64, i64, p, p]
+        lib.fp8o_quant_act_ue8m0.argtypes = [p, i64, i64, i64, i64, p, p]
+        lib.fp8o_quant_weight_ue8m0.argtypes = [p, i64, i64, i64, i64, p, p]
         lib.fp8o_block_partials.argtypes = [p, p, i64, i64, i64, p]
         lib.fp8o_gemm.argtypes = [p, p, p, p, i64, p, i64, p, i64, p, p]
         lib.fp8o_wgrad_gemm.argtypes = [p, p, p, p, i64, p, i64, p, i64, p, p]
@@ -148,6 +150,49 @@ def quant_weight(w_bits, threads: int | None = None):
         list(ex.map(lambda c: lib.fp8o_quant_weight(_ptr(w), N, K, c[0], c[1], _ptr(q), _ptr(s)),
                     chunks))
     return q, s
+
+
+def quant_act_ue8m0(x_bits, threads: int | None = None):
+    """1x128 tiles with power-of-two (UE8M0) scales: (codes uint8 [M, K],
+    scale bytes uint8 [M, ceil(K/128)]; the scale is 2^(byte - 127))."""
+    lib = _load()
+    x = _as_bf16_bits(x_bits)
+    M, K = x.shape
+    q = np.empty((M, K), dtype=np.uint8)
+    s = np.empty((M, -(-K // TILE)), dtype=np.uint8)
+    chunks = _split(M, _threads(threads))
+    with ThreadPoolExecutor(len(chunks)) as ex:
+        list(ex.map(lambda c: lib.fp8o_quant_act_ue8m0(_ptr(x), M, K, c[0], c[1], _ptr(q), _ptr(s)),
+                    chunks))
+    return q, s
+
+
+def quant_weight_ue8m0(w_bits, threads: int | None = None):
+    """128x128 blocks with power-of-two (UE8M0) scales: (codes uint8 [N, K],
+    scale bytes uint8 [ceil(N/128), ceil(K/128)])."""
+    lib = _load()
+    w = _as_bf16_bits(w_bits)
+    N, K = w.shape
+    q = np.empty((N, K), dtype=np.uint8)
+    s = np.empty((-(-N // TILE), -(-K // TILE)), dtype=np.uint8)
+    chunks = _split(-(-N // TILE), _threads(threads))
+    with ThreadPoolExecutor(len(chunks)) as ex:
+        list(ex.map(lambda c: lib.fp8o_quant_weight_ue8m0(_ptr(w), N, K, c[0], c[1], _ptr(q), _ptr(s)),
+                    chunks))
+    return q, s
+
+
+def ue8m0_to_f32(s_bytes) -> np.ndarray:
+    """The scale a UE8M0 byte stands for: 2^(byte - 127), exact in float32
+    (2^-127 is a float32 subnormal)."""
+    b = np.asarray(s_bytes, dtype=np.int32)
+    return np.ldexp(np.float32(1.0), b - 127).astype(np.float32)
+
+
+def gemm_ue8m0(qa, sa_bytes, qb, sb_bytes, rows=None, cols=None, threads: int | None = None):
+    """The block-scaled GEMM with UE8M0 scales: by definition the same
+    computation as gemm() with the scales 2^(byte - 127)."""
+    return gemm(qa, ue8m0_to_f32(sa_bytes), qb, ue8m0_to_f32(sb_bytes), rows, cols, threads)
 
 
 def quant_act_t(x_bits, threads: int | None = None):

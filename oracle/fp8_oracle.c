@@ -176,6 +176,80 @@ void fp8o_quant_weight(const uint16_t* w, int64_t N, int64_t K, int64_t nb_begin
 }
 
 /*
+ * Power-of-two (UE8M0) scales: a variant that the pages do not describe. It
+ * keeps the 1x128 / 128x128 granularity but rounds each scale up to a power
+ * of two, so that a tensor core with block scaling in hardware (8-bit
+ * exponent scale factors) can apply it:
+ *   e = ceil(log2(amax / 448)), the smallest integer with amax / 2^e <= 448,
+ *   stored as the byte e + 127 (clamped below at 0, i.e. 2^-127);
+ *   q = E4M3_RNE_sat(fl32(x / 2^e)); an all-zero tile gets byte 0, codes 0.
+ * With amax = f * 2^E (frexp, f in [0.5, 1)) and 448 = 0.875 * 2^9, the
+ * ratio amax / 448 = (f / 0.875) * 2^(E - 9) lies in (2^(E - 10), 2^(E - 8)),
+ * so e = E - 9 when f <= 0.875 and E - 8 otherwise (exact comparisons).
+ */
+static uint8_t ue8m0_scale_byte(float amax) {
+    if (amax == 0.0f) return 0;
+    int E;
+    double f = frexp((double)amax, &E);
+    int e = f > 0.875 ? E - 8 : E - 9;
+    if (e < -127) e = -127;
+    return (uint8_t)(e + 127);
+}
+
+static uint8_t encode_pow2(float x, uint8_t sbyte, int zero_tile) {
+    if (zero_tile) return 0x00;
+    float s = ldexpf(1.0f, (int)sbyte - 127); /* exact, 2^-127 is an fp32 subnormal */
+    return fp8o_e4m3_encode(x / s);
+}
+
+/* 1x128 tiles with UE8M0 scales; s: uint8 [M, ceil(K/128)]. */
+void fp8o_quant_act_ue8m0(const uint16_t* x, int64_t M, int64_t K, int64_t m_begin,
+                          int64_t m_end, uint8_t* q, uint8_t* s) {
+    (void)M;
+    int64_t KB = (K + TILE - 1) / TILE;
+    for (int64_t m = m_begin; m < m_end; ++m) {
+        for (int64_t kb = 0; kb < KB; ++kb) {
+            int64_t k0 = kb * TILE;
+            int64_t k1 = k0 + TILE < K ? k0 + TILE : K;
+            float amax = 0.0f;
+            for (int64_t k = k0; k < k1; ++k) {
+                float v = fabsf(bf16_to_f32(x[m * K + k]));
+                if (v > amax) amax = v;
+            }
+            uint8_t sb = ue8m0_scale_byte(amax);
+            s[m * KB + kb] = sb;
+            for (int64_t k = k0; k < k1; ++k)
+                q[m * K + k] = encode_pow2(bf16_to_f32(x[m * K + k]), sb, amax == 0.0f);
+        }
+    }
+}
+
+/* 128x128 blocks with UE8M0 scales; s: uint8 [ceil(N/128), ceil(K/128)]. */
+void fp8o_quant_weight_ue8m0(const uint16_t* w, int64_t N, int64_t K, int64_t nb_begin,
+                             int64_t nb_end, uint8_t* q, uint8_t* s) {
+    int64_t KB = (K + TILE - 1) / TILE;
+    for (int64_t nb = nb_begin; nb < nb_end; ++nb) {
+        int64_t n0 = nb * TILE;
+        int64_t n1 = n0 + TILE < N ? n0 + TILE : N;
+        for (int64_t kb = 0; kb < KB; ++kb) {
+            int64_t k0 = kb * TILE;
+            int64_t k1 = k0 + TILE < K ? k0 + TILE : K;
+            float amax = 0.0f;
+            for (int64_t n = n0; n < n1; ++n)
+                for (int64_t k = k0; k < k1; ++k) {
+                    float v = fabsf(bf16_to_f32(w[n * K + k]));
+                    if (v > amax) amax = v;
+                }
+            uint8_t sb = ue8m0_scale_byte(amax);
+            s[nb * KB + kb] = sb;
+            for (int64_t n = n0; n < n1; ++n)
+                for (int64_t k = k0; k < k1; ++k)
+                    q[n * K + k] = encode_pow2(bf16_to_f32(w[n * K + k]), sb, amax == 0.0f);
+        }
+    }
+}
+
+/*
  * The exact per-K-block partial P_kb[m, n] = sum_{k in block kb} dec(qa[m,k]) *
  * dec(qb[n,k]) for kb = 0..ceil(K/128)-1, written to P[kb].
  * Exactness: every E4M3 value is an integer below 2^18 times 2^-9, so each
