@@ -18,7 +18,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libfp8q.so")
-SOURCES = ["api.cu", "quant.cu", "gemm.cu"]
+SOURCES = ["api.cu", "quant.cu", "gemm.cu", "gemm_bs.cu"]
 HEADERS = ["ptx.cuh", "gemm.cuh", "quant.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

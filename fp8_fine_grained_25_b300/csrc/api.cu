@@ -148,36 +148,41 @@ int fp8q_set_gemm_pairs(int enable) {
 
 int fp8q_get_device_status(cudaStream_t stream, uint32_t* status_out, int clear) {
     if (!status_out) return FP8Q_ERR_NULL;
-    uint32_t gemm_status = 0, quant_status = 0;
+    uint32_t gemm_status = 0, quant_status = 0, bs_status = 0;
     if (fp8q::read_device_status(stream, &gemm_status, clear != 0) != cudaSuccess ||
-        fp8q::read_quant_status(&quant_status, clear != 0) != cudaSuccess)
+        fp8q::read_quant_status(&quant_status, clear != 0) != cudaSuccess ||
+        fp8q::read_bs_status(&bs_status, clear != 0) != cudaSuccess)
         return FP8Q_ERR_CUDA;
-    *status_out = gemm_status | quant_status;
+    *status_out = gemm_status | quant_status | bs_status;
     return FP8Q_OK;
 }
 
-int fp8q_quant_act(const void* x_bf16, int64_t M, int64_t K, void* q_e4m3, float* scales,
+}  // extern "C"
+
+namespace {
+
+int quant_act_impl(const void* x_bf16, int64_t M, int64_t K, void* q_e4m3, void* scales, bool pow2,
                    cudaStream_t stream) {
     if (M < 0 || K <= 0 || M > kI32Max || K > kI32Max) return FP8Q_ERR_SHAPE;
     if (M == 0) return FP8Q_OK;
     if (!x_bf16 || !q_e4m3 || !scales) return FP8Q_ERR_NULL;
-    if (K % 16 != 0 || !aligned(x_bf16, 16) || !aligned(q_e4m3, 16) || !aligned(scales, 4))
+    if (K % 16 != 0 || !aligned(x_bf16, 16) || !aligned(q_e4m3, 16) || !aligned(scales, pow2 ? 1 : 4))
         return FP8Q_ERR_ALIGN;
     if (M * cdiv(K, 128) > kI32Max) return FP8Q_ERR_SHAPE;
     DeviceInfo* dev = nullptr;
     if (int rc = current_device(&dev)) return rc;
-    return fp8q::launch_quant_act(x_bf16, M, K, q_e4m3, scales, stream, dev->sms, g_timeout_ns) ==
+    return fp8q::launch_quant_act(x_bf16, M, K, q_e4m3, scales, pow2, stream, dev->sms, g_timeout_ns) ==
                    cudaSuccess
                ? FP8Q_OK
                : FP8Q_ERR_CUDA;
 }
 
-int fp8q_quant_weight(const void* w_bf16, int64_t N, int64_t K, void* q_e4m3, float* scales,
+int quant_weight_impl(const void* w_bf16, int64_t N, int64_t K, void* q_e4m3, void* scales, bool pow2,
                       cudaStream_t stream) {
     if (N < 0 || K <= 0 || N > kI32Max || K > kI32Max) return FP8Q_ERR_SHAPE;
     if (N == 0) return FP8Q_OK;
     if (!w_bf16 || !q_e4m3 || !scales) return FP8Q_ERR_NULL;
-    if (K % 16 != 0 || !aligned(w_bf16, 16) || !aligned(q_e4m3, 16) || !aligned(scales, 4))
+    if (K % 16 != 0 || !aligned(w_bf16, 16) || !aligned(q_e4m3, 16) || !aligned(scales, pow2 ? 1 : 4))
         return FP8Q_ERR_ALIGN;
     DeviceInfo* dev = nullptr;
     if (int rc = current_device(&dev)) return rc;
@@ -185,10 +190,34 @@ int fp8q_quant_weight(const void* w_bf16, int64_t N, int64_t K, void* q_e4m3, fl
     if (!make_map_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w_bf16, K, N, 128, 128,
                      CU_TENSOR_MAP_SWIZZLE_NONE))
         return FP8Q_ERR_CUDA;
-    return fp8q::launch_quant_weight(&tmW, q_e4m3, scales, N, K, stream, dev->sms,
-                                     g_timeout_ns) == cudaSuccess
+    return fp8q::launch_quant_weight(&tmW, q_e4m3, scales, pow2, N, K, stream, dev->sms, g_timeout_ns) ==
+                   cudaSuccess
                ? FP8Q_OK
                : FP8Q_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fp8q_quant_act(const void* x_bf16, int64_t M, int64_t K, void* q_e4m3, float* scales,
+                   cudaStream_t stream) {
+    return quant_act_impl(x_bf16, M, K, q_e4m3, scales, false, stream);
+}
+
+int fp8q_quant_weight(const void* w_bf16, int64_t N, int64_t K, void* q_e4m3, float* scales,
+                      cudaStream_t stream) {
+    return quant_weight_impl(w_bf16, N, K, q_e4m3, scales, false, stream);
+}
+
+int fp8q_quant_act_ue8m0(const void* x_bf16, int64_t M, int64_t K, void* q_e4m3, uint8_t* scales,
+                         cudaStream_t stream) {
+    return quant_act_impl(x_bf16, M, K, q_e4m3, scales, true, stream);
+}
+
+int fp8q_quant_weight_ue8m0(const void* w_bf16, int64_t N, int64_t K, void* q_e4m3, uint8_t* scales,
+                            cudaStream_t stream) {
+    return quant_weight_impl(w_bf16, N, K, q_e4m3, scales, true, stream);
 }
 
 int fp8q_quant_act_t(const void* x_bf16, int64_t M, int64_t K, void* qt_e4m3, float* st,
@@ -328,6 +357,30 @@ int fp8_block_gemm(const void* A, const float* sa, const void* B, const float* s
 int fp8_wgrad_gemm(const void* A, const float* sa, const void* B, const float* sb, void* C_bf16,
                    int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
     return dense_gemm(A, sa, B, sb, C_bf16, M, N, K, true, stream);
+}
+
+int fp8_block_gemm_ue8m0(const void* A, const uint8_t* sa, const void* B, const uint8_t* sb,
+                         void* C_bf16, int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
+    if (M < 0 || N <= 0 || K <= 0 || M > kI32Max || N > kI32Max || K > kI32Max)
+        return FP8Q_ERR_SHAPE;
+    if (M == 0) return FP8Q_OK;
+    if (!A || !sa || !B || !sb || !C_bf16) return FP8Q_ERR_NULL;
+    if (K % 16 != 0 || N % 8 != 0 || !aligned(A, 16) || !aligned(B, 16) || !aligned(C_bf16, 16))
+        return FP8Q_ERR_ALIGN;
+    DeviceInfo* dev = nullptr;
+    if (int rc = current_device(&dev)) return rc;
+    CUtensorMap tmA, tmB, tmC;
+    if (!make_map_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, K, M, 128, 128) ||
+        !make_map_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, K, N, 128,
+                     static_cast<uint32_t>(fp8q::gemm_bs_tile_n())) ||
+        !make_map_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C_bf16, N, M, 32, 32,
+                     CU_TENSOR_MAP_SWIZZLE_64B))
+        return FP8Q_ERR_CUDA;
+    return fp8q::launch_gemm_bs(&tmA, &tmB, &tmC, sa, sb, static_cast<int32_t>(M), static_cast<int32_t>(N),
+                                static_cast<int32_t>(K), g_timeout_ns, g_inject, dev->sms, stream) ==
+                   cudaSuccess
+               ? FP8Q_OK
+               : FP8Q_ERR_CUDA;
 }
 
 int fp8_grouped_gemm(const void* A, const float* sa, const void* B, const float* sb,

@@ -352,6 +352,49 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                  : "memory");
 }
 
+// D[tmem] (+)= (A * 2^(sfA - 127)) * (B * 2^(sfB - 127))^T with the block
+// scale factors applied by the tensor core: kind::mxf8f6f4.block_scale,
+// one 8-bit exponent (UE8M0) scale per row of A and per column of B for the
+// instruction's 32-wide K slice. The scale factors are read from tensor
+// memory: for the A rows 32 j + r (j = 0..3) at column sfa_tmem + j, lane r
+// of each 32-lane quarter, and for the B columns 32 j + r at column
+// sfb_tmem + j likewise; the byte of the 32-bit cell is chosen by the
+// scale-factor ids in the instruction descriptor.
+__device__ __forceinline__ void mma_e4m3_bs(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem),
+        "r"(accumulate)
+        : "memory");
+}
+
+// Instruction descriptor for kind::mxf8f6f4 with E4M3 A and B and UE8M0
+// scale factors: [4,6) B scale-factor byte id, [7,10) / [10,13) A / B
+// format (0 = E4M3), bits 15/16 A/B major (0 = K), [17,23) N >> 3, bit 23
+// scale format (1 = UE8M0), [24,29) M >> 4, [29,31) A scale-factor byte id.
+__host__ __device__ constexpr uint32_t idesc_e4m3_bs(int M, int N, uint32_t a_sf_id, uint32_t b_sf_id) {
+    return (b_sf_id << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) |
+           (static_cast<uint32_t>(M >> 4) << 24) | (a_sf_id << 29);
+}
+
+// 16 consecutive 32-bit TMEM columns of this warp's 32 lanes (lane i of the
+// warp writes lane i of its quarter); visible to later tcgen05 operations
+// after tmem_wait_st and a tcgen05 fence around the synchronising barrier.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // Instruction descriptor for kind::f8f6f4 with E4M3 A and B, FP32 D, both
 // operands K-major, dense. Fields: [4,6) D format (1 = F32), [7,10) A
 // format (0 = E4M3), [10,13) B format (0 = E4M3), bit 15/16 A/B major

@@ -116,6 +116,41 @@ __device__ __forceinline__ float tile_scale(float amax) {
     return __fmaf_rn(-e, r448, q0);
 }
 
+// Power-of-two (UE8M0) scales: the byte e + 127 of the smallest power of two
+// 2^e with amax / 2^e <= 448, clamped below at 0. With amax's fp32 exponent
+// field E8 and mantissa field m, amax / 448 = (1.m / 1.75) * 2^(E8 - 135), so
+// e = E8 - 135 when 1.m <= 1.75 and E8 - 134 otherwise; subnormal and zero
+// amax clamp to byte 0.
+__device__ __forceinline__ uint32_t ue8m0_byte(float amax) {
+    const uint32_t b = __float_as_uint(amax);
+    const int v = static_cast<int>((b >> 23) & 0xFFu) - 8 + ((b & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+    return v < 0 ? 0u : static_cast<uint32_t>(v);
+}
+// 2^(byte - 127) (2^-127 is an fp32 subnormal) and 2^(127 - byte), byte <= 253
+__device__ __forceinline__ float pow2_of_byte(uint32_t byte) {
+    return byte == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(byte << 23);
+}
+__device__ __forceinline__ float inv_pow2_of_byte(uint32_t byte) { return __uint_as_float((254u - byte) << 23); }
+
+// The tile's scale, reciprocal and fast-path flag for encode8_r. POW2: the
+// UE8M0 scale, for which x * 2^-e is exact, so the correction step of
+// div_by_scale is zero and the fast path always applies; all-zero tiles get
+// s = 0 (codes 0) and byte 0.
+template <bool POW2>
+__device__ __forceinline__ void tile_scale_for(float amax, float& sc, float& r, bool& fast, uint32_t& byte) {
+    if constexpr (POW2) {
+        byte = ue8m0_byte(amax);
+        sc = amax == 0.0f ? 0.0f : pow2_of_byte(byte);
+        r = inv_pow2_of_byte(byte);
+        fast = true;
+    } else {
+        sc = tile_scale(amax);
+        fast = amax >= kFastDivMinAmax;
+        r = fast ? __frcp_rn(sc) : 0.0f;
+        byte = 0;
+    }
+}
+
 // Eight values of a tile whose scale s and reciprocal r = RN(1/s) (or 0 for
 // the IEEE-divide range, amax < 2^-90) are known, encoded low byte first.
 // PACKED runs the quotients two lanes per instruction (same results); the
@@ -178,7 +213,8 @@ constexpr int kActSmem = kActStages * kActStageBytes + 8 * (2 * kActStages) + 16
 struct ActArgs {
     const uint8_t* x;  // bf16 [M, K]
     uint8_t* q;        // [M, K]
-    float* s;          // [M, KB]
+    float* s;          // [M, KB] fp32 scales
+    uint8_t* s8;       // [M, KB] UE8M0 scale bytes (POW2)
     int64_t K;
     uint32_t T, KB;
     uint32_t nchunks;
@@ -190,7 +226,8 @@ __device__ __forceinline__ int64_t tile_start(int64_t t, uint32_t KB, int64_t K)
     return m * K + (t - m * KB) * 128;
 }
 
-template <bool FLAT>  // FLAT: K % 128 == 0, tile t starts at element 128 t
+// FLAT: K % 128 == 0, tile t starts at element 128 t; POW2: UE8M0 scales
+template <bool FLAT, bool POW2>
 __global__ void __launch_bounds__(kActThreads, 1) quant_act_kernel(const ActArgs a) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -286,15 +323,19 @@ __global__ void __launch_bounds__(kActThreads, 1) quant_act_kernel(const ActArgs
             bits = max(bits, __shfl_xor_sync(0xFFFFFFFFu, bits, 1));
             bits = max(bits, __shfl_xor_sync(0xFFFFFFFFu, bits, 2));
             const float amax = __uint_as_float(bits << 16);
-            const float sc = tile_scale(amax);
-            const bool fast = amax >= kFastDivMinAmax;
-            const float r = fast ? __frcp_rn(sc) : 0.0f;
+            float sc, r;
+            bool fast;
+            uint32_t byte;
+            tile_scale_for<POW2>(amax, sc, r, fast, byte);
             if (live) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
                     if (8 * chunk[j] < len)
                         *reinterpret_cast<uint2*>(a.q + base + 8 * chunk[j]) = encode8_r<false>(v[j], sc, r, fast);
-                if (sub == 0) a.s[t] = sc;
+                if (sub == 0) {
+                    if constexpr (POW2) a.s8[t] = static_cast<uint8_t>(byte);
+                    else a.s[t] = sc;
+                }
             }
             if (++stage == kActStages) {
                 stage = 0;
@@ -326,12 +367,14 @@ static_assert(kWStages % kWGroups == 0, "each group must cycle through its own s
 
 struct WeightArgs {
     uint8_t* q;  // [N, K]
-    float* s;    // [NB, KB]
+    float* s;    // [NB, KB] fp32 scales
+    uint8_t* s8; // [NB, KB] UE8M0 scale bytes (POW2)
     int64_t N, K;
     uint32_t NB, KB;
     uint64_t timeout_ns;
 };
 
+template <bool POW2>  // POW2: UE8M0 scales
 __global__ void __launch_bounds__(kWThreads, 1)
     quant_weight_kernel(const __grid_constant__ CUtensorMap tmW, const WeightArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -423,9 +466,10 @@ __global__ void __launch_bounds__(kWThreads, 1)
             float amax = rb[0];
 #pragma unroll
             for (int i = 1; i < kWGroupWarps; ++i) amax = fmaxf(amax, rb[i]);
-            const float sc = tile_scale(amax);
-            const bool fast = amax >= kFastDivMinAmax;
-            const float r = fast ? __frcp_rn(sc) : 0.0f;
+            float sc, r;
+            bool fast;
+            uint32_t byte;
+            tile_scale_for<POW2>(amax, sc, r, fast, byte);
             const int64_t k = static_cast<int64_t>(kb) * 128 + 8 * (tid & 15u);
             const int64_t n0 = static_cast<int64_t>(nb) * 128 + (tid >> 4);
 #pragma unroll
@@ -434,7 +478,10 @@ __global__ void __launch_bounds__(kWThreads, 1)
                 if (n < a.N && k < a.K)
                     *reinterpret_cast<uint2*>(a.q + n * a.K + k) = encode8_r<true>(v[j], sc, r, fast);
             }
-            if (tid == 0) a.s[b] = sc;
+            if (tid == 0) {
+                if constexpr (POW2) a.s8[b] = static_cast<uint8_t>(byte);
+                else a.s[b] = sc;
+            }
             stage += kWGroups;
             if (stage >= kWStages) {
                 stage -= kWStages;
@@ -766,37 +813,38 @@ cudaError_t launch_gather_rows(const void* q_src, const float* s_src, int64_t T,
     return cudaGetLastError();
 }
 
-cudaError_t launch_quant_act(const void* x, int64_t M, int64_t K, void* q, float* s,
+template <bool FLAT, bool POW2>
+cudaError_t launch_act(const ActArgs& a, unsigned grid, cudaStream_t stream) {
+    cudaError_t err = cudaFuncSetAttribute(quant_act_kernel<FLAT, POW2>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, kActSmem);
+    if (err != cudaSuccess) return err;
+    quant_act_kernel<FLAT, POW2><<<grid, kActThreads, kActSmem, stream>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_act(const void* x, int64_t M, int64_t K, void* q, void* s, bool pow2,
                              cudaStream_t stream, int num_sms, uint64_t timeout_ns) {
     ActArgs a;
     a.x = static_cast<const uint8_t*>(x);
     a.q = static_cast<uint8_t*>(q);
-    a.s = s;
+    a.s = pow2 ? nullptr : static_cast<float*>(s);
+    a.s8 = pow2 ? static_cast<uint8_t*>(s) : nullptr;
     a.K = K;
     a.KB = static_cast<uint32_t>((K + 127) / 128);
     a.T = static_cast<uint32_t>(M * a.KB);
     a.nchunks = (a.T + kActChunkTiles - 1) / kActChunkTiles;
     a.timeout_ns = timeout_ns;
     const unsigned grid = a.nchunks < static_cast<uint32_t>(num_sms) ? a.nchunks : num_sms;
-    if (K % 128 == 0) {
-        cudaError_t err = cudaFuncSetAttribute(quant_act_kernel<true>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, kActSmem);
-        if (err != cudaSuccess) return err;
-        quant_act_kernel<true><<<grid, kActThreads, kActSmem, stream>>>(a);
-    } else {
-        cudaError_t err = cudaFuncSetAttribute(quant_act_kernel<false>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, kActSmem);
-        if (err != cudaSuccess) return err;
-        quant_act_kernel<false><<<grid, kActThreads, kActSmem, stream>>>(a);
-    }
-    return cudaGetLastError();
+    if (K % 128 == 0) return pow2 ? launch_act<true, true>(a, grid, stream) : launch_act<true, false>(a, grid, stream);
+    return pow2 ? launch_act<false, true>(a, grid, stream) : launch_act<false, false>(a, grid, stream);
 }
 
-cudaError_t launch_quant_weight(const CUtensorMap* tmW, void* q, float* s, int64_t N, int64_t K,
-                                cudaStream_t stream, int num_sms, uint64_t timeout_ns) {
+cudaError_t launch_quant_weight(const CUtensorMap* tmW, void* q, void* s, bool pow2, int64_t N,
+                                int64_t K, cudaStream_t stream, int num_sms, uint64_t timeout_ns) {
     WeightArgs a;
     a.q = static_cast<uint8_t*>(q);
-    a.s = s;
+    a.s = pow2 ? nullptr : static_cast<float*>(s);
+    a.s8 = pow2 ? static_cast<uint8_t*>(s) : nullptr;
     a.N = N;
     a.K = K;
     a.NB = static_cast<uint32_t>((N + 127) / 128);
@@ -804,10 +852,10 @@ cudaError_t launch_quant_weight(const CUtensorMap* tmW, void* q, float* s, int64
     a.timeout_ns = timeout_ns;
     const uint64_t nblocks = static_cast<uint64_t>(a.NB) * a.KB;
     const unsigned grid = static_cast<unsigned>(nblocks < static_cast<uint64_t>(num_sms) ? nblocks : num_sms);
-    cudaError_t err =
-        cudaFuncSetAttribute(quant_weight_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kWSmem);
+    auto kern = pow2 ? quant_weight_kernel<true> : quant_weight_kernel<false>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kWSmem);
     if (err != cudaSuccess) return err;
-    quant_weight_kernel<<<grid, kWThreads, kWSmem, stream>>>(*tmW, a);
+    kern<<<grid, kWThreads, kWSmem, stream>>>(*tmW, a);
     return cudaGetLastError();
 }
 

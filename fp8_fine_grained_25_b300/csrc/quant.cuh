@@ -7,11 +7,12 @@
 
 namespace fp8q {
 
-cudaError_t launch_quant_act(const void* x, int64_t M, int64_t K, void* q, float* s,
+// s: fp32 scales, or UE8M0 scale bytes when pow2
+cudaError_t launch_quant_act(const void* x, int64_t M, int64_t K, void* q, void* s, bool pow2,
                              cudaStream_t stream, int num_sms, uint64_t timeout_ns);
 // tmW: bf16 [N, K] tensor map, box 128 x 128, no swizzle
-cudaError_t launch_quant_weight(const CUtensorMap* tmW, void* q, float* s, int64_t N, int64_t K,
-                                cudaStream_t stream, int num_sms, uint64_t timeout_ns);
+cudaError_t launch_quant_weight(const CUtensorMap* tmW, void* q, void* s, bool pow2, int64_t N,
+                                int64_t K, cudaStream_t stream, int num_sms, uint64_t timeout_ns);
 // w: bf16 [N, K] (N % 16 == 0, K % 16 == 0); writes qt [K, N] and st
 // [KB, NB], and q [N, K] and s [NB, KB] unless q is null
 cudaError_t launch_quant_weight_t(const void* w, void* q, float* s, void* qt, float* st, int64_t N,

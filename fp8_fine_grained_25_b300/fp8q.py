@@ -24,9 +24,12 @@ _i64, _i32, _p = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p
 lib.fp8q_quant_act.argtypes = [_p, _i64, _i64, _p, _p, _p]
 lib.fp8q_quant_weight.argtypes = [_p, _i64, _i64, _p, _p, _p]
 lib.fp8q_quant_act_t.argtypes = [_p, _i64, _i64, _p, _p, _p]
+lib.fp8q_quant_act_ue8m0.argtypes = [_p, _i64, _i64, _p, _p, _p]
+lib.fp8q_quant_weight_ue8m0.argtypes = [_p, _i64, _i64, _p, _p, _p]
 lib.fp8q_quant_weight_t.argtypes = [_p, _i64, _i64, _p, _p, _p, _p, _p]
 lib.fp8_block_gemm.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p]
 lib.fp8_wgrad_gemm.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p]
+lib.fp8_block_gemm_ue8m0.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p]
 lib.fp8q_gather_rows.argtypes = [_p, _p, _i64, _i64, _p, _i64, _p, _p, _p]
 lib.fp8q_gather_rows.restype = ctypes.c_int
 lib.fp8_grouped_gemm.argtypes = [_p, _p, _p, _p, _p, _p, _i32, _i64, _i64, _i64, _p]
@@ -42,7 +45,9 @@ lib.fp8q_set_fault_injection.restype = ctypes.c_int
 lib.fp8q_status_string.argtypes = [ctypes.c_int]
 lib.fp8q_status_string.restype = ctypes.c_char_p
 for _f in ("fp8q_quant_act", "fp8q_quant_weight", "fp8q_quant_act_t", "fp8q_quant_weight_t",
-           "fp8_block_gemm", "fp8_wgrad_gemm", "fp8_grouped_gemm", "fp8q_get_device_status"):
+           "fp8q_quant_act_ue8m0", "fp8q_quant_weight_ue8m0",
+           "fp8_block_gemm", "fp8_wgrad_gemm", "fp8_block_gemm_ue8m0", "fp8_grouped_gemm",
+           "fp8q_get_device_status"):
     getattr(lib, _f).restype = ctypes.c_int
 
 OK, ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_DEVICE, ERR_CUDA, ERR_TIMEOUT, ERR_UNSUPPORTED, ERR_OFFSETS = range(9)
@@ -131,6 +136,40 @@ def fp8q_quant_weight(w: torch.Tensor, q: torch.Tensor | None = None,
     _need(scales, "scales", (torch.float32,), sshape)
     _check(lib.fp8q_quant_weight(w.data_ptr(), rows, K, q.data_ptr(), scales.data_ptr(),
                                  _stream(stream)), "fp8q_quant_weight")
+    return q, scales
+
+
+def fp8q_quant_act_ue8m0(x: torch.Tensor, q: torch.Tensor | None = None,
+                         scales: torch.Tensor | None = None, stream=None):
+    """1x128 tiles with power-of-two (UE8M0) scales -> (q uint8 [M, K], scale
+    bytes uint8 [M, ceil(K/128)]; the scale is 2^(byte - 127))."""
+    M, K = x.shape
+    _need(x, "x", (torch.bfloat16,), None)
+    if q is None:
+        q = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty((M, _cdiv(K, 128)), dtype=torch.uint8, device=x.device)
+    _need(q, "q", CODE_DTYPES, (M, K))
+    _need(scales, "scales", (torch.uint8,), (M, _cdiv(K, 128)))
+    _check(lib.fp8q_quant_act_ue8m0(x.data_ptr(), M, K, q.data_ptr(), scales.data_ptr(),
+                                    _stream(stream)), "fp8q_quant_act_ue8m0")
+    return q, scales
+
+
+def fp8q_quant_weight_ue8m0(w: torch.Tensor, q: torch.Tensor | None = None,
+                            scales: torch.Tensor | None = None, stream=None):
+    """128x128 blocks with power-of-two (UE8M0) scales -> (q uint8 [N, K], scale
+    bytes uint8 [ceil(N/128), ceil(K/128)])."""
+    N, K = w.shape
+    _need(w, "w", (torch.bfloat16,), None)
+    if q is None:
+        q = torch.empty((N, K), dtype=torch.uint8, device=w.device)
+    if scales is None:
+        scales = torch.empty((_cdiv(N, 128), _cdiv(K, 128)), dtype=torch.uint8, device=w.device)
+    _need(q, "q", CODE_DTYPES, (N, K))
+    _need(scales, "scales", (torch.uint8,), (_cdiv(N, 128), _cdiv(K, 128)))
+    _check(lib.fp8q_quant_weight_ue8m0(w.data_ptr(), N, K, q.data_ptr(), scales.data_ptr(),
+                                       _stream(stream)), "fp8q_quant_weight_ue8m0")
     return q, scales
 
 
@@ -236,6 +275,24 @@ def fp8_wgrad_gemm(A: torch.Tensor, sa: torch.Tensor, B: torch.Tensor, sb: torch
     _need(C, "C", (torch.bfloat16,), (M, N))
     _check(lib.fp8_wgrad_gemm(A.data_ptr(), sa.data_ptr(), B.data_ptr(), sb.data_ptr(),
                               C.data_ptr(), M, N, K, _stream(stream)), "fp8_wgrad_gemm")
+    return C
+
+
+def fp8_block_gemm_ue8m0(A: torch.Tensor, sa: torch.Tensor, B: torch.Tensor, sb: torch.Tensor,
+                         C: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """C[M, N] (bf16) = A[M, K] * B[N, K]^T with UE8M0 scale bytes (sa [M, KB],
+    sb [NB, KB]) applied by the tensor core."""
+    M, K = A.shape
+    N = B.shape[0]
+    _need(A, "A", CODE_DTYPES, (M, K))
+    _need(B, "B", CODE_DTYPES, (N, K))
+    _need(sa, "sa", (torch.uint8,), (M, _cdiv(K, 128)))
+    _need(sb, "sb", (torch.uint8,), (_cdiv(N, 128), _cdiv(K, 128)))
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    _need(C, "C", (torch.bfloat16,), (M, N))
+    _check(lib.fp8_block_gemm_ue8m0(A.data_ptr(), sa.data_ptr(), B.data_ptr(), sb.data_ptr(),
+                                    C.data_ptr(), M, N, K, _stream(stream)), "fp8_block_gemm_ue8m0")
     return C
 
 

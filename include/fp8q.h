@@ -98,6 +98,25 @@ FP8Q_API int fp8q_quant_weight(const void* w_bf16, int64_t N, int64_t K, void* q
                       cudaStream_t stream);
 
 /*
+ * Power-of-two (UE8M0) scales: the same 1x128 / 128x128 tiles with each
+ * scale rounded up to a power of two, the form that a tensor core with
+ * hardware block scaling applies (8-bit exponent scale factors). The pages
+ * do not describe this variant.
+ *   scale byte = e + 127 with e = ceil(log2(amax / 448)) (the smallest power
+ *   of two with amax / 2^e <= 448), clamped below at 0; the scale is
+ *   2^(byte - 127). Codes q = E4M3_rn_satfinite(x / 2^e) (an exact quotient).
+ *   An all-zero tile gets byte 0 and all-zero codes.
+ *   fp8q_quant_act_ue8m0:    x [M, K] -> q [M, K], scales uint8 [M, ceil(K/128)]
+ *   fp8q_quant_weight_ue8m0: w [N, K] -> q [N, K], scales uint8 [ceil(N/128), ceil(K/128)]
+ * Same alignment and error rules as fp8q_quant_act / fp8q_quant_weight,
+ * except that the byte scales need no alignment.
+ */
+FP8Q_API int fp8q_quant_act_ue8m0(const void* x_bf16, int64_t M, int64_t K, void* q_e4m3,
+                                  uint8_t* scales, cudaStream_t stream);
+FP8Q_API int fp8q_quant_weight_ue8m0(const void* w_bf16, int64_t N, int64_t K, void* q_e4m3,
+                                     uint8_t* scales, cudaStream_t stream);
+
+/*
  * Activation quantization for the weight gradient: 128x1 tiles (128
  * consecutive rows of one column, i.e. 1x128 tiles along the token axis of
  * x^T), written transposed so that the tokens become the contraction axis
@@ -161,6 +180,22 @@ FP8Q_API int fp8q_gather_rows(const void* q_src, const float* s_src, int64_t T, 
  */
 FP8Q_API int fp8_block_gemm(const void* A, const float* sa, const void* B, const float* sb, void* C_bf16,
                    int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+
+/*
+ * The block-scaled FP8 GEMM with power-of-two (UE8M0) scales from
+ * fp8q_quant_act_ue8m0 / fp8q_quant_weight_ue8m0 (a variant the pages do not
+ * describe). The tensor core applies the scales itself (block-scaled MMA,
+ * one scale per row of A / column of B per 32-wide K slice) and accumulates
+ * the whole K range in FP32, so there is no promotion through registers.
+ *   A  in : E4M3 codes [M, K]     sa in: UE8M0 bytes [M, ceil(K/128)]
+ *   B  in : E4M3 codes [N, K]     sb in: UE8M0 bytes [ceil(N/128), ceil(K/128)]
+ *   C  out: bf16 [M, N] = bf16_rn( sum_k dec(A[m][k]) 2^(sa - 127) dec(B[n][k]) 2^(sb - 127) )
+ * Accuracy: within 1 bf16 ulp + 1e-5 * sum_k |a_k b_k| of the block-wise FP32
+ * definition (fp8_block_gemm with the scales 2^(byte - 127)). Alignment and
+ * errors as fp8_block_gemm; the byte scales need no alignment.
+ */
+FP8Q_API int fp8_block_gemm_ue8m0(const void* A, const uint8_t* sa, const void* B, const uint8_t* sb,
+                                  void* C_bf16, int64_t M, int64_t N, int64_t K, cudaStream_t stream);
 
 /*
  * Grouped (per-expert) block-scaled FP8 GEMM for the MoE FFN (news.qq.com

@@ -190,3 +190,16 @@ def test_wgrad_gemm_argument_checks(lib):
         assert _wg(lib, *args, 128, 256, 512, None) == NULL
     assert _wg(lib, P, P, P, P, P, 128, 256, 520, None) == ALIGN
     assert _wg(lib, P, P, P, P, P, 128, 252, 512, None) == ALIGN
+
+
+def test_ue8m0_quantizer_argument_checks(lib):
+    for name in ("fp8q_quant_act_ue8m0", "fp8q_quant_weight_ue8m0"):
+        f = getattr(lib, name)
+        f.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+                      ctypes.c_void_p, ctypes.c_void_p]
+        assert f(P, -1, 128, P, P, None) == SHAPE
+        assert f(None, 0, 128, None, None, None) == OK
+        assert f(P, 4, 128, P, None, None) == NULL
+        assert f(P, 4, 120, P, P, None) == ALIGN
+        assert f(P, 4, 128, P + 8, P, None) == ALIGN
+        assert f(P, 4, 128, P, P + 1, None) != ALIGN  # byte scales need no alignment
