@@ -26,6 +26,7 @@ struct DeviceInfo {
     // ([0]: 128, [1]: 256) and B-scale layout ([0]: 128x128 blocks, [1]: one
     // per row); -1: not queried yet
     int pair_clusters[2][2] = {{-1, -1}, {-1, -1}};
+    int bs_pair_clusters = -1;  // the same for the UE8M0 (hardware-scaled) GEMM
 };
 
 constexpr int kMaxDevices = 64;
@@ -369,16 +370,22 @@ int fp8_block_gemm_ue8m0(const void* A, const uint8_t* sa, const void* B, const 
         return FP8Q_ERR_ALIGN;
     DeviceInfo* dev = nullptr;
     if (int rc = current_device(&dev)) return rc;
+    bool pair = g_pair_mode && M > 128;
+    if (pair) {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        if (dev->bs_pair_clusters < 0) dev->bs_pair_clusters = fp8q::gemm_bs_pair_max_clusters();
+        pair = dev->bs_pair_clusters > 0;
+    }
+    const uint32_t bn = static_cast<uint32_t>(fp8q::gemm_bs_tile_n());
     CUtensorMap tmA, tmB, tmC;
     if (!make_map_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, K, M, 128, 128) ||
-        !make_map_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, K, N, 128,
-                     static_cast<uint32_t>(fp8q::gemm_bs_tile_n())) ||
+        !make_map_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, K, N, 128, pair ? bn / 2 : bn) ||
         !make_map_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C_bf16, N, M, 32, 32,
                      CU_TENSOR_MAP_SWIZZLE_64B))
         return FP8Q_ERR_CUDA;
     return fp8q::launch_gemm_bs(&tmA, &tmB, &tmC, sa, sb, static_cast<int32_t>(M), static_cast<int32_t>(N),
-                                static_cast<int32_t>(K), g_timeout_ns, g_inject, dev->sms, stream) ==
-                   cudaSuccess
+                                static_cast<int32_t>(K), pair, dev->bs_pair_clusters, g_timeout_ns, g_inject,
+                                dev->sms, stream) == cudaSuccess
                ? FP8Q_OK
                : FP8Q_ERR_CUDA;
 }

@@ -372,6 +372,22 @@ __device__ __forceinline__ void mma_e4m3_bs(uint32_t d_tmem, uint64_t a_desc, ui
         : "memory");
 }
 
+// 2-CTA form (issued by one thread of the even CTA): each CTA supplies its
+// 128 rows of A and half of B's rows from its shared memory; each CTA's
+// tensor memory holds the scale factors of its own A rows and of all N
+// columns of B (the same column layout), at the same addresses.
+__device__ __forceinline__ void mma_e4m3_bs_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                 uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                 uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem),
+        "r"(accumulate)
+        : "memory");
+}
+
 // Instruction descriptor for kind::mxf8f6f4 with E4M3 A and B and UE8M0
 // scale factors: [4,6) B scale-factor byte id, [7,10) / [10,13) A / B
 // format (0 = E4M3), bits 15/16 A/B major (0 = K), [17,23) N >> 3, bit 23

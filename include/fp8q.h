@@ -258,7 +258,7 @@ FP8Q_API void fp8q_set_wait_timeout_ns(uint64_t ns);
 FP8Q_API int fp8q_set_gemm_tile_n(int bn);
 
 /*
- * Whether fp8_block_gemm and fp8_wgrad_gemm may run an output tile of
+ * Whether fp8_block_gemm, fp8_wgrad_gemm and fp8_block_gemm_ue8m0 may run an output tile of
  * 256 rows on a pair of SMs (2-CTA clusters with the 2-CTA tensor-core MMA,
  * each SM holding half of the B tile). 1 (the default) uses pairs whenever
  * M > 128, for both tile widths; 0 keeps one SM per 128 x N tile. Affects
@@ -269,7 +269,7 @@ FP8Q_API int fp8q_set_gemm_pairs(int enable);
 /*
  * Failure injection for tests of the device-side failure path. With
  * FP8Q_INJECT_STALLED_STAGE set, every fp8_block_gemm / fp8_wgrad_gemm /
- * fp8_grouped_gemm launch announces 16 more bytes for its first pipeline stage than the
+ * fp8_block_gemm_ue8m0 / fp8_grouped_gemm launch announces 16 more bytes for its first pipeline stage than the
  * stage receives, so that stage never completes: the kernel's bounded waits
  * expire (see fp8q_set_wait_timeout_ns), it drains its copies, frees its
  * tensor memory, writes nothing further, returns, and the device status word

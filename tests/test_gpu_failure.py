@@ -95,3 +95,27 @@ def test_wgrad_stalled_stage_times_out(q, pairs):
     assert q.fp8q_get_device_status() == 0
     c32, S = oracle.wgrad_gemm(qa, sa, qb, sb)
     assert_gemm_ok(to_f32(C), c32, S, "weight-gradient GEMM after an injected timeout")
+
+
+@pytest.mark.parametrize("pairs", [True, False])
+def test_ue8m0_gemm_stalled_stage_times_out(q, pairs):
+    # the hardware-scaled GEMM has its own pipeline (scale-factor ring in
+    # tensor memory): a stalled stage must unwind it as well
+    q.fp8q_set_gemm_pairs(pairs)
+    rng = np.random.default_rng(8)
+    t = lambda a: torch.from_numpy(a).to(DEV)
+    M, N, K = 512, 448, 1024
+    qa = rng.choice(FINITE, size=(M, K)).astype(np.uint8)
+    qb = rng.choice(FINITE, size=(N, K)).astype(np.uint8)
+    sa = rng.integers(118, 136, size=(M, K // 128)).astype(np.uint8)
+    sb = rng.integers(118, 136, size=(-(-N // 128), K // 128)).astype(np.uint8)
+    q.fp8q_set_wait_timeout_ns(20_000_000)
+    q.fp8q_set_fault_injection(q.INJECT_STALLED_STAGE)
+    q.fp8_block_gemm_ue8m0(t(qa), t(sa), t(qb), t(sb))
+    assert q.fp8q_get_device_status() & q.DEVSTATUS_TIMEOUT
+    q.fp8q_set_fault_injection(0)
+    q.fp8q_set_wait_timeout_ns(0)
+    C = q.fp8_block_gemm_ue8m0(t(qa), t(sa), t(qb), t(sb))
+    assert q.fp8q_get_device_status() == 0
+    c32, S = oracle.gemm_ue8m0(qa, sa, qb, sb)
+    assert_gemm_ok(to_f32(C), c32, S, "UE8M0 GEMM after an injected timeout")

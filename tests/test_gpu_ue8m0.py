@@ -90,18 +90,23 @@ def _run_bs(q, qa, sa, qb, sb):
 
 
 BS_SHAPES = [(128, 224, 128), (1, 8, 16), (300, 520, 400), (129, 264, 144), (257, 576, 7168),
-             (640, 1536, 1024), (1000, 2056, 256), (384, 448, 2048)]
+             (640, 1536, 1024), (1000, 2056, 256), (384, 448, 2048), (512, 224, 640)]
 
 
+@pytest.mark.parametrize("pairs", [True, False])
 @pytest.mark.parametrize("M,N,K", BS_SHAPES)
-def test_block_gemm_ue8m0_random_codes(q, M, N, K):
+def test_block_gemm_ue8m0_random_codes(q, M, N, K, pairs):
     rng = np.random.default_rng(M + 3 * N + 7 * K)
     KB, NB = -(-K // 128), -(-N // 128)
     qa = rng.choice(FINITE, size=(M, K)).astype(np.uint8)
     qb = rng.choice(FINITE, size=(N, K)).astype(np.uint8)
     sa = rng.integers(110, 140, size=(M, KB)).astype(np.uint8)
     sb = rng.integers(110, 140, size=(NB, KB)).astype(np.uint8)
-    C = _run_bs(q, qa, sa, qb, sb)
+    q.fp8q_set_gemm_pairs(pairs)
+    try:
+        C = _run_bs(q, qa, sa, qb, sb)
+    finally:
+        q.fp8q_set_gemm_pairs(True)
     c32, S = oracle.gemm_ue8m0(qa, sa, qb, sb)
     from gpu_helpers import assert_gemm_ok, to_f32
     assert not np.isnan(to_f32(C)).any(), "unwritten outputs"
