@@ -182,8 +182,10 @@ class Path:
         self.w = w
         A = w.A
         M, K = A.shape
+        self.ue8m0 = w.scales == "ue8m0"
+        sdt = torch.uint8 if self.ue8m0 else torch.float32  # UE8M0 scale bytes or fp32 scales
         self.qa = torch.empty((M, K), dtype=torch.uint8, device=device)
-        self.sa = torch.empty((M, -(-K // 128)), dtype=torch.float32, device=device)
+        self.sa = torch.empty((M, -(-K // 128)), dtype=sdt, device=device)
         self.bufs = {}
         for name, W in w.weights.items():
             qb = torch.empty(W.shape, dtype=torch.uint8, device=device)
@@ -192,8 +194,7 @@ class Path:
                                  device=device)
                 C = torch.empty((M, W.shape[1]), dtype=torch.bfloat16, device=device)
             else:
-                sb = torch.empty((-(-W.shape[0] // 128), -(-K // 128)), dtype=torch.float32,
-                                 device=device)
+                sb = torch.empty((-(-W.shape[0] // 128), -(-K // 128)), dtype=sdt, device=device)
                 C = torch.empty((M, W.shape[0]), dtype=torch.bfloat16, device=device)
             self.bufs[name] = (qb, sb, C)
         self.launches_per_step = 1 + 2 * len(w.weights)
@@ -212,6 +213,7 @@ class Path:
         self.dominant_flops = self.flops
         self.describe = (w.name + ": quant_act(A) + quant_weight(W) + "
                          + ("grouped" if w.offsets is not None else "dense")
+                         + (" hardware-scaled" if self.ue8m0 else "")
                          + " block-scaled GEMM per step")
 
     def inputs(self):
@@ -232,13 +234,18 @@ class Path:
         if self.dispatch:
             f.fp8q_quant_act(A, self.qx, self.sx, stream=stream)
             f.fp8q_gather_rows(self.qx, self.sx, self.w.index, self.qa, self.sa, stream=stream)
+        elif self.ue8m0:
+            f.fp8q_quant_act_ue8m0(A, self.qa, self.sa, stream=stream)
         else:
             f.fp8q_quant_act(A, self.qa, self.sa, stream=stream)
         rec(1)
         i = 2
         for name in self.w.weights:
             qb, sb, _ = self.bufs[name]
-            f.fp8q_quant_weight(inp[name], qb, sb, stream=stream)
+            if self.ue8m0:
+                f.fp8q_quant_weight_ue8m0(inp[name], qb, sb, stream=stream)
+            else:
+                f.fp8q_quant_weight(inp[name], qb, sb, stream=stream)
             rec(i)
             i += 1
         for name in self.w.weights:
@@ -247,6 +254,8 @@ class Path:
                 C = outs[name]
             if self.w.offsets is not None:
                 f.fp8_grouped_gemm(self.qa, self.sa, qb, sb, self.w.offsets, C, stream=stream)
+            elif self.ue8m0:
+                f.fp8_block_gemm_ue8m0(self.qa, self.sa, qb, sb, C, stream=stream)
             else:
                 f.fp8_block_gemm(self.qa, self.sa, qb, sb, C, stream=stream)
             rec(i)
@@ -376,13 +385,16 @@ def oracle_sample(w, rows_a: int, rows_b: int, out_rows: int, threads: int):
     bits = lambda t: t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
     a_s = bits(A[:rows_a])
     b_s = bits(Wd[:rows_b])
+    pow2 = w.scales == "ue8m0"
+    qact = oracle.quant_act_ue8m0 if pow2 else oracle.quant_act
+    qweight = oracle.quant_weight_ue8m0 if pow2 else oracle.quant_weight
+    gemm = oracle.gemm_ue8m0 if pow2 else oracle.gemm
     t0 = time.perf_counter()
-    qa, sa = oracle.quant_act(a_s, threads=threads)
+    qa, sa = qact(a_s, threads=threads)
     t1 = time.perf_counter()
-    qb_full, sb_full = oracle.quant_weight(bits(Wd), threads=threads)  # GEMM needs all of B
+    qb_full, sb_full = qweight(bits(Wd), threads=threads)  # GEMM needs all of B
     t2 = time.perf_counter()
-    c32, S = oracle.gemm(qa, sa, qb_full, sb_full, rows=np.arange(min(out_rows, rows_a)),
-                         threads=threads)
+    c32, S = gemm(qa, sa, qb_full, sb_full, rows=np.arange(min(out_rows, rows_a)), threads=threads)
     t3 = time.perf_counter()
     w_elems = sum(W.numel() for W in w.weights.values())
     full = ((t1 - t0) * (M * K) / a_s.size
@@ -474,7 +486,7 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5, 6, 7, 8])
+    ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5, 6, 7, 8, 9])
     ap.add_argument("--e2e-steps", type=int, default=10)
     args = ap.parse_args()
     if args.warmup < 3:
@@ -548,6 +560,9 @@ def main():
         traffic = profiled_traffic("gemm_dense_8192x7168x7168.md", "gemm.cu")
         kernel_profiles = {"quant_act": ("quant_act_8192x7168.md", "quant.cu"),
                            "quant_weight[B]": ("quant_weight_7168x7168.md", "quant.cu")}
+    elif args.config == 9:
+        traffic = profiled_traffic("gemm_ue8m0_dense_8192x7168x7168.md", "gemm_bs.cu")
+        kernel_profiles = {"quant_act": ("quant_ue8m0_8192x7168.md", "quant.cu")}
     elif args.config == 8:
         traffic = profiled_traffic("gemm_wgrad_7168x7168x8192.md", "gemm.cu")
         kernel_profiles = {"quant_act[dY]": ("quant_act_8192x7168.md", "quant.cu"),
@@ -561,7 +576,8 @@ def main():
                 "frac": gemm_tflops / fp8_peak, "traffic": traffic,
                 "traffic_unit": "DRAM bytes per launch (ncu, profiles/)",
                 "frac_of_burst_peak": gemm_tflops / fp8_burst,
-                "kernel": "fp8_gemm_kernel " + "+".join(path.dominant), "peak_source":
+                "kernel": ("fp8_gemm_bs_kernel " if getattr(path, "ue8m0", False) else "fp8_gemm_kernel ")
+                          + "+".join(path.dominant), "peak_source":
                     f"{peak_kind} bf16 sustained {sustained} TFLOP/s x {FP8_OVER_BF16} "
                     f"(nominal FP8:BF16 ratio); burst {peaks['bf16_tflops']} x {FP8_OVER_BF16} = "
                     f"{fp8_burst:.1f}"}

@@ -79,6 +79,7 @@ class Workload:
     tokens: torch.Tensor | None = None    # MoE: the un-gathered token activations [T, K]
     index: torch.Tensor | None = None     # MoE: int32 token of each routed row (A = tokens[index])
     X: torch.Tensor | None = None         # backward: the layer input [T, K] (A holds dY [T, N])
+    scales: str = "fp32"                  # "fp32" (amax / 448) or "ue8m0" (powers of two)
 
 
 def tiny(seed: int = 0, device="cpu") -> Workload:
@@ -160,5 +161,14 @@ def dense_backward(seed: int = 0, device="cpu", T: int = 8192) -> Workload:
                     note="A holds dY; X is the layer input", X=X)
 
 
+def dense_square_ue8m0(seed: int = 0, device="cpu", M: int = 8192) -> Workload:
+    """dense_square's tensors, quantized with power-of-two (UE8M0) scales and
+    multiplied by the hardware-scaled GEMM."""
+    w = dense_square(seed, device, M)
+    w.name = f"dense {M}x7168x7168, UE8M0 scales"
+    w.scales = "ue8m0"
+    return w
+
+
 CONFIGS = {1: tiny, 2: mla_down, 3: dense_square, 4: moe_grouped, 5: large_m, 6: mla_down_fused,
-           7: moe_dispatch_fp8, 8: dense_backward}
+           7: moe_dispatch_fp8, 8: dense_backward, 9: dense_square_ue8m0}
