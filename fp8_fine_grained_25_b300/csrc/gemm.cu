@@ -333,16 +333,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true, issued_any = false;
             for (int t = unit0; ok && t < num_tiles; t += unit_step) {
                 for (int kb = 0; kb < KB; ++kb) {
-                    if (!warp_wait<PAIR>(bar(L::TEMPTY + abuf), aphase ^ 1u, abort_flag, limit) ||
-                        !warp_wait<PAIR>(bar(L::FULL + stage), phase, abort_flag, limit)) {
+                    // the operands usually land long before the accumulator
+                    // buffer is released: wait for them first, so that only
+                    // the release stands between the promotion and the MMA
+                    if (!warp_wait<PAIR>(bar(L::FULL + stage), phase, abort_flag, limit)) {
                         ok = false;
                         break;
                     }
-                    tc_fence_after_sync();
                     const uint32_t sA = sbase + stage * L::STAGE_BYTES;
                     const uint64_t ad = sdesc_k_sw128(sA);
                     const uint64_t bd = sdesc_k_sw128(sA + L::A_BYTES);
                     const uint32_t d = tmem_base + abuf * BN;
+                    if (!warp_wait<PAIR>(bar(L::TEMPTY + abuf), aphase ^ 1u, abort_flag, limit)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
                     if (elect_one()) {
                         if constexpr (PAIR) {
 #pragma unroll
