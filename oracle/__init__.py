@@ -195,6 +195,26 @@ def gemm_ue8m0(qa, sa_bytes, qb, sb_bytes, rows=None, cols=None, threads: int | 
     return gemm(qa, ue8m0_to_f32(sa_bytes), qb, ue8m0_to_f32(sb_bytes), rows, cols, threads)
 
 
+def quant_act_t_ue8m0(x_bits, threads: int | None = None):
+    """128x1 tiles (along M) with UE8M0 scales, written transposed: the 1x128
+    UE8M0 tiles of x^T. Returns (codes uint8 [K, M], bytes uint8 [K, ceil(M/128)])."""
+    x = _as_bf16_bits(x_bits)
+    return quant_act_ue8m0(np.ascontiguousarray(x.T), threads)
+
+
+def quant_weight_t_ue8m0(w_bits, threads: int | None = None):
+    """128x128 UE8M0 blocks in both layouts: (q [N, K], s [NB, KB], qt [K, N],
+    st [KB, NB]); a block's byte and codes do not depend on the orientation."""
+    q, s = quant_weight_ue8m0(w_bits, threads)
+    return q, s, np.ascontiguousarray(q.T), np.ascontiguousarray(s.T)
+
+
+def wgrad_gemm_ue8m0(qa, sa_bytes, qb, sb_bytes, rows=None, cols=None, threads: int | None = None):
+    """The weight-gradient GEMM with UE8M0 row scales on both operands: by
+    definition wgrad_gemm() with the scales 2^(byte - 127)."""
+    return wgrad_gemm(qa, ue8m0_to_f32(sa_bytes), qb, ue8m0_to_f32(sb_bytes), rows, cols, threads)
+
+
 def quant_act_t(x_bits, threads: int | None = None):
     """Quantization of bf16 activations [M, K] in 128x1 tiles (128 consecutive
     rows of one column), written transposed: the 1x128 tiles of x^T.

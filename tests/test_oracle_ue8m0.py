@@ -112,3 +112,44 @@ def test_ue8m0_gemm_fraction_brute_force():
             # the per-block scaling is exact; only the FP32 roundings of the
             # two block terms and their sum remain
             assert abs(Fraction(float(c32[m, n])) - exact) <= Fraction(3 * 2.0 ** -24) * Se
+
+
+def test_act_t_ue8m0_bytes_follow_the_rule_per_column_tile():
+    # 128x1 tiles along M: byte[k, mb] is the smallest 2^e with
+    # max_{m in block} |x[m, k]| / 2^e <= 448, checked exactly from x
+    rng = np.random.default_rng(9)
+    M, K = 300, 48
+    x = _bf16(rng.standard_normal((M, K)) * np.exp2(rng.integers(-30, 30, size=(1, K))))
+    qt, st = oracle.quant_act_t_ue8m0(_bits(x))
+    assert qt.shape == (K, M) and st.shape == (K, 3)
+    xf = x.float().numpy().astype(np.float64)
+    for k in range(K):
+        for mb in range(3):
+            amax = Fraction(float(np.abs(xf[128 * mb:min(M, 128 * mb + 128), k]).max()))
+            sc = Fraction(2) ** (int(st[k, mb]) - 127)
+            assert amax / sc <= 448 < amax / (sc / 2)
+    # codes: the exact quotients through the library codec
+    scale = np.repeat(oracle.ue8m0_to_f32(st), 128, axis=1)[:, :M]
+    ref = (xf.T.astype(np.float32) / scale).astype(ml_dtypes.float8_e4m3fn).view(np.uint8)
+    assert np.array_equal(qt, ref)
+
+
+def test_wgrad_ue8m0_fraction_brute_force():
+    rng = np.random.default_rng(10)
+    M, N, K = 3, 4, 256
+    qa = rng.choice(FINITE, size=(M, K)).astype(np.uint8)
+    qb = rng.choice(FINITE, size=(N, K)).astype(np.uint8)
+    sa = rng.integers(110, 145, size=(M, 2)).astype(np.uint8)
+    sb = rng.integers(110, 145, size=(N, 2)).astype(np.uint8)  # one byte per B row
+    c32, S = oracle.wgrad_gemm_ue8m0(qa, sa, qb, sb)
+    dec = lambda c: Fraction(float(oracle.e4m3_decode(np.array([c], np.uint8))[0]))
+    for m in range(M):
+        for n in range(N):
+            exact, Se = Fraction(0), Fraction(0)
+            for kb in range(2):
+                sc = Fraction(2) ** (int(sa[m, kb]) + int(sb[n, kb]) - 254)
+                for k in range(128 * kb, 128 * kb + 128):
+                    t = dec(qa[m, k]) * dec(qb[n, k]) * sc
+                    exact += t
+                    Se += abs(t)
+            assert abs(Fraction(float(c32[m, n])) - exact) <= Fraction(3 * 2.0 ** -24) * Se
