@@ -301,11 +301,12 @@ class BackwardPath:
         T, N = dY.shape
         K = X.shape[1]
         e = lambda *shape, dt=torch.uint8: torch.empty(shape, dtype=dt, device=device)
-        f32 = torch.float32
-        self.qdy, self.sdy = e(T, N), e(T, -(-N // 128), dt=f32)
-        self.qwt, self.swt = e(K, N), e(-(-K // 128), -(-N // 128), dt=f32)
-        self.qdyt, self.sdyt = e(N, T), e(N, -(-T // 128), dt=f32)
-        self.qxt, self.sxt = e(K, T), e(K, -(-T // 128), dt=f32)
+        self.ue8m0 = w.scales == "ue8m0"
+        sdt = torch.uint8 if self.ue8m0 else torch.float32  # UE8M0 bytes or fp32 scales
+        self.qdy, self.sdy = e(T, N), e(T, -(-N // 128), dt=sdt)
+        self.qwt, self.swt = e(K, N), e(-(-K // 128), -(-N // 128), dt=sdt)
+        self.qdyt, self.sdyt = e(N, T), e(N, -(-T // 128), dt=sdt)
+        self.qxt, self.sxt = e(K, T), e(K, -(-T // 128), dt=sdt)
         self.dX = e(T, K, dt=torch.bfloat16)
         self.dW = e(N, K, dt=torch.bfloat16)
         self.T, self.N, self.K = T, N, K
@@ -332,17 +333,22 @@ class BackwardPath:
         outs = self.outputs() if outs is None else outs
         rec = (lambda i: events[i].record(stream)) if events is not None else (lambda i: None)
         rec(0)
-        f.fp8q_quant_act(inp["dY"], self.qdy, self.sdy, stream=stream)
+        u = self.ue8m0
+        (f.fp8q_quant_act_ue8m0 if u else f.fp8q_quant_act)(inp["dY"], self.qdy, self.sdy, stream=stream)
         rec(1)
-        f.fp8q_quant_weight_t(inp["W"], qt=self.qwt, st=self.swt, with_forward=False, stream=stream)
+        (f.fp8q_quant_weight_t_ue8m0 if u else f.fp8q_quant_weight_t)(
+            inp["W"], qt=self.qwt, st=self.swt, with_forward=False, stream=stream)
         rec(2)
-        f.fp8_block_gemm(self.qdy, self.sdy, self.qwt, self.swt, outs["dX"], stream=stream)
+        (f.fp8_block_gemm_ue8m0 if u else f.fp8_block_gemm)(self.qdy, self.sdy, self.qwt, self.swt,
+                                                            outs["dX"], stream=stream)
         rec(3)
-        f.fp8q_quant_act_t(inp["dY"], self.qdyt, self.sdyt, stream=stream)
+        act_t = f.fp8q_quant_act_t_ue8m0 if u else f.fp8q_quant_act_t
+        act_t(inp["dY"], self.qdyt, self.sdyt, stream=stream)
         rec(4)
-        f.fp8q_quant_act_t(inp["X"], self.qxt, self.sxt, stream=stream)
+        act_t(inp["X"], self.qxt, self.sxt, stream=stream)
         rec(5)
-        f.fp8_wgrad_gemm(self.qdyt, self.sdyt, self.qxt, self.sxt, outs["dW"], stream=stream)
+        (f.fp8_wgrad_gemm_ue8m0 if u else f.fp8_wgrad_gemm)(self.qdyt, self.sdyt, self.qxt, self.sxt,
+                                                            outs["dW"], stream=stream)
         rec(6)
 
     def kernels(self, per):
@@ -418,18 +424,24 @@ def oracle_sample_backward(w, rows: int, cols: int, out_rows: int, threads: int)
     K = X.shape[1]
     bits = lambda t: t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
     dy_rows, dy_cols, x_cols, w_bits = bits(dY[:rows]), bits(dY[:, :cols]), bits(X[:, :cols]), bits(W)
+    u = w.scales == "ue8m0"
+    qact = oracle.quant_act_ue8m0 if u else oracle.quant_act
+    qwt = oracle.quant_weight_t_ue8m0 if u else oracle.quant_weight_t
+    gemm = oracle.gemm_ue8m0 if u else oracle.gemm
+    qact_t = oracle.quant_act_t_ue8m0 if u else oracle.quant_act_t
+    wgrad = oracle.wgrad_gemm_ue8m0 if u else oracle.wgrad_gemm
     t = [time.perf_counter()]
-    qdy, sdy = oracle.quant_act(dy_rows, threads=threads)
+    qdy, sdy = qact(dy_rows, threads=threads)
     t.append(time.perf_counter())
-    _, _, qwt, swt = oracle.quant_weight_t(w_bits, threads=threads)
+    _, _, qwt_, swt_ = qwt(w_bits, threads=threads)
     t.append(time.perf_counter())
-    oracle.gemm(qdy, sdy, qwt, swt, rows=np.arange(out_rows), threads=threads)
+    gemm(qdy, sdy, qwt_, swt_, rows=np.arange(out_rows), threads=threads)
     t.append(time.perf_counter())
-    qdyt, sdyt = oracle.quant_act_t(dy_cols, threads=threads)
+    qdyt, sdyt = qact_t(dy_cols, threads=threads)
     t.append(time.perf_counter())
-    qxt, sxt = oracle.quant_act_t(x_cols, threads=threads)
+    qxt, sxt = qact_t(x_cols, threads=threads)
     t.append(time.perf_counter())
-    oracle.wgrad_gemm(qdyt, sdyt, qxt, sxt, rows=np.arange(out_rows), threads=threads)
+    wgrad(qdyt, sdyt, qxt, sxt, rows=np.arange(out_rows), threads=threads)
     t.append(time.perf_counter())
     d = np.diff(t)
     full = (d[0] * T / rows + d[1] + d[2] * T / out_rows + d[3] * N / cols + d[4] * K / cols
@@ -486,7 +498,7 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5, 6, 7, 8, 9])
+    ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5, 6, 7, 8, 9, 10])
     ap.add_argument("--e2e-steps", type=int, default=10)
     args = ap.parse_args()
     if args.warmup < 3:

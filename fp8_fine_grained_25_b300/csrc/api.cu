@@ -26,7 +26,7 @@ struct DeviceInfo {
     // ([0]: 128, [1]: 256) and B-scale layout ([0]: 128x128 blocks, [1]: one
     // per row); -1: not queried yet
     int pair_clusters[2][2] = {{-1, -1}, {-1, -1}};
-    int bs_pair_clusters = -1;  // the same for the UE8M0 (hardware-scaled) GEMM
+    int bs_pair_clusters[2] = {-1, -1};  // the same for the UE8M0 (hardware-scaled) GEMM
 };
 
 constexpr int kMaxDevices = 64;
@@ -221,38 +221,67 @@ int fp8q_quant_weight_ue8m0(const void* w_bf16, int64_t N, int64_t K, void* q_e4
     return quant_weight_impl(w_bf16, N, K, q_e4m3, scales, true, stream);
 }
 
-int fp8q_quant_act_t(const void* x_bf16, int64_t M, int64_t K, void* qt_e4m3, float* st,
+}  // extern "C"
+
+namespace {
+
+int quant_act_t_impl(const void* x_bf16, int64_t M, int64_t K, void* qt_e4m3, void* st, bool pow2,
                      cudaStream_t stream) {
     if (M < 0 || K <= 0 || M > kI32Max || K > kI32Max) return FP8Q_ERR_SHAPE;
     if (M == 0) return FP8Q_OK;
     if (!x_bf16 || !qt_e4m3 || !st) return FP8Q_ERR_NULL;
     if (K % 16 != 0 || M % 16 != 0 || !aligned(x_bf16, 16) || !aligned(qt_e4m3, 16) ||
-        !aligned(st, 4))
+        !aligned(st, pow2 ? 1 : 4))
         return FP8Q_ERR_ALIGN;
     DeviceInfo* dev = nullptr;
     if (int rc = current_device(&dev)) return rc;
     if (cdiv(M, 128) * cdiv(K, 128) > kI32Max) return FP8Q_ERR_SHAPE;
-    return fp8q::launch_quant_act_t(x_bf16, qt_e4m3, st, M, K, stream, dev->sms) == cudaSuccess
+    return fp8q::launch_quant_act_t(x_bf16, qt_e4m3, st, pow2, M, K, stream, dev->sms) == cudaSuccess
                ? FP8Q_OK
                : FP8Q_ERR_CUDA;
 }
 
-int fp8q_quant_weight_t(const void* w_bf16, int64_t N, int64_t K, void* q_e4m3, float* scales,
-                        void* qt_e4m3, float* st, cudaStream_t stream) {
+int quant_weight_t_impl(const void* w_bf16, int64_t N, int64_t K, void* q_e4m3, void* scales,
+                        void* qt_e4m3, void* st, bool pow2, cudaStream_t stream) {
     if (N < 0 || K <= 0 || N > kI32Max || K > kI32Max) return FP8Q_ERR_SHAPE;
     if (N == 0) return FP8Q_OK;
     if (!w_bf16 || !qt_e4m3 || !st || (q_e4m3 == nullptr) != (scales == nullptr))
         return FP8Q_ERR_NULL;
+    const uintptr_t sal = pow2 ? 1 : 4;
     if (K % 16 != 0 || N % 16 != 0 || !aligned(w_bf16, 16) || !aligned(qt_e4m3, 16) ||
-        !aligned(st, 4) || (q_e4m3 && !aligned(q_e4m3, 16)) || (scales && !aligned(scales, 4)))
+        !aligned(st, sal) || (q_e4m3 && !aligned(q_e4m3, 16)) || (scales && !aligned(scales, sal)))
         return FP8Q_ERR_ALIGN;
     DeviceInfo* dev = nullptr;
     if (int rc = current_device(&dev)) return rc;
     if (cdiv(N, 128) * cdiv(K, 128) > kI32Max) return FP8Q_ERR_SHAPE;
-    return fp8q::launch_quant_weight_t(w_bf16, q_e4m3, scales, qt_e4m3, st, N, K, stream, dev->sms) ==
+    return fp8q::launch_quant_weight_t(w_bf16, q_e4m3, scales, qt_e4m3, st, pow2, N, K, stream, dev->sms) ==
                    cudaSuccess
                ? FP8Q_OK
                : FP8Q_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fp8q_quant_act_t(const void* x_bf16, int64_t M, int64_t K, void* qt_e4m3, float* st,
+                     cudaStream_t stream) {
+    return quant_act_t_impl(x_bf16, M, K, qt_e4m3, st, false, stream);
+}
+
+int fp8q_quant_weight_t(const void* w_bf16, int64_t N, int64_t K, void* q_e4m3, float* scales,
+                        void* qt_e4m3, float* st, cudaStream_t stream) {
+    return quant_weight_t_impl(w_bf16, N, K, q_e4m3, scales, qt_e4m3, st, false, stream);
+}
+
+int fp8q_quant_act_t_ue8m0(const void* x_bf16, int64_t M, int64_t K, void* qt_e4m3, uint8_t* st,
+                           cudaStream_t stream) {
+    return quant_act_t_impl(x_bf16, M, K, qt_e4m3, st, true, stream);
+}
+
+int fp8q_quant_weight_t_ue8m0(const void* w_bf16, int64_t N, int64_t K, void* q_e4m3, uint8_t* scales,
+                              void* qt_e4m3, uint8_t* st, cudaStream_t stream) {
+    return quant_weight_t_impl(w_bf16, N, K, q_e4m3, scales, qt_e4m3, st, true, stream);
 }
 
 int fp8q_gather_rows(const void* q_src, const float* s_src, int64_t T, int64_t K,
@@ -360,8 +389,12 @@ int fp8_wgrad_gemm(const void* A, const float* sa, const void* B, const float* s
     return dense_gemm(A, sa, B, sb, C_bf16, M, N, K, true, stream);
 }
 
-int fp8_block_gemm_ue8m0(const void* A, const uint8_t* sa, const void* B, const uint8_t* sb,
-                         void* C_bf16, int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+int gemm_ue8m0_impl(const void* A, const uint8_t* sa, const void* B, const uint8_t* sb, void* C_bf16,
+                    int64_t M, int64_t N, int64_t K, bool row_scaled_b, cudaStream_t stream) {
     if (M < 0 || N <= 0 || K <= 0 || M > kI32Max || N > kI32Max || K > kI32Max)
         return FP8Q_ERR_SHAPE;
     if (M == 0) return FP8Q_OK;
@@ -371,10 +404,11 @@ int fp8_block_gemm_ue8m0(const void* A, const uint8_t* sa, const void* B, const 
     DeviceInfo* dev = nullptr;
     if (int rc = current_device(&dev)) return rc;
     bool pair = g_pair_mode && M > 128;
+    int* pc = &dev->bs_pair_clusters[row_scaled_b ? 1 : 0];
     if (pair) {
         std::lock_guard<std::mutex> lock(g_mutex);
-        if (dev->bs_pair_clusters < 0) dev->bs_pair_clusters = fp8q::gemm_bs_pair_max_clusters();
-        pair = dev->bs_pair_clusters > 0;
+        if (*pc < 0) *pc = fp8q::gemm_bs_pair_max_clusters(row_scaled_b);
+        pair = *pc > 0;
     }
     const uint32_t bn = static_cast<uint32_t>(fp8q::gemm_bs_tile_n());
     CUtensorMap tmA, tmB, tmC;
@@ -384,10 +418,24 @@ int fp8_block_gemm_ue8m0(const void* A, const uint8_t* sa, const void* B, const 
                      CU_TENSOR_MAP_SWIZZLE_64B))
         return FP8Q_ERR_CUDA;
     return fp8q::launch_gemm_bs(&tmA, &tmB, &tmC, sa, sb, static_cast<int32_t>(M), static_cast<int32_t>(N),
-                                static_cast<int32_t>(K), pair, dev->bs_pair_clusters, g_timeout_ns, g_inject,
+                                static_cast<int32_t>(K), row_scaled_b, pair, *pc, g_timeout_ns, g_inject,
                                 dev->sms, stream) == cudaSuccess
                ? FP8Q_OK
                : FP8Q_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fp8_block_gemm_ue8m0(const void* A, const uint8_t* sa, const void* B, const uint8_t* sb,
+                         void* C_bf16, int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
+    return gemm_ue8m0_impl(A, sa, B, sb, C_bf16, M, N, K, false, stream);
+}
+
+int fp8_wgrad_gemm_ue8m0(const void* A, const uint8_t* sa, const void* B, const uint8_t* sb,
+                         void* C_bf16, int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
+    return gemm_ue8m0_impl(A, sa, B, sb, C_bf16, M, N, K, true, stream);
 }
 
 int fp8_grouped_gemm(const void* A, const float* sa, const void* B, const float* sb,

@@ -49,11 +49,13 @@ cudaError_t read_device_status(cudaStream_t stream, uint32_t* out, bool clear);
 // output tiles of 128 x gemm_bs_tile_n() per CTA; tmB's box is that many
 // rows, or half of them in pair mode (2-CTA clusters, 256-row tiles).
 int gemm_bs_tile_n();
-int gemm_bs_pair_max_clusters();
+// row_scaled_b: sb holds one UE8M0 byte per row of B ([N][KB]) instead of
+// one per 128-row block
+int gemm_bs_pair_max_clusters(bool row_scaled_b);
 cudaError_t launch_gemm_bs(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmC,
                            const uint8_t* sa, const uint8_t* sb, int32_t M, int32_t N, int32_t K,
-                           bool pair, int pair_clusters, uint64_t timeout_ns, uint32_t debug, int num_sms,
-                           cudaStream_t stream);
+                           bool row_scaled_b, bool pair, int pair_clusters, uint64_t timeout_ns,
+                           uint32_t debug, int num_sms, cudaStream_t stream);
 cudaError_t read_bs_status(uint32_t* out, bool clear);
 
 }  // namespace fp8q

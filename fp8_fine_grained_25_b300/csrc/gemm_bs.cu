@@ -125,7 +125,9 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
-template <bool PAIR>
+// ROWB: one scale per row of B (sb [N][KB], the weight-gradient layout)
+// instead of one per 128-row block.
+template <bool PAIR, bool ROWB>
 __global__ void __launch_bounds__(kThreads, 1)
     fp8_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmC, const BsArgs args) {
@@ -325,8 +327,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < kBN / 32; ++j) {
                 const int n = n0 + 32 * j + lane;
-                v[kSfbOff + j] =
-                    n < args.N ? cell(args.sb + static_cast<int64_t>(n >> 7) * KB, 4 * g) : 0x7F7F7F7Fu;
+                const int64_t brow = ROWB ? n : (n >> 7);
+                v[kSfbOff + j] = n < args.N ? cell(args.sb + brow * KB, 4 * g) : 0x7F7F7F7Fu;
             }
 #pragma unroll
             for (int j = kSfbOff + kBN / 32; j < 16; ++j) v[j] = 0x7F7F7F7Fu;
@@ -430,11 +432,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0 && *abort_flag) atomicOr(&g_bs_status, FP8Q_DEVSTATUS_TIMEOUT);
 }
 
-template <bool PAIR>
+template <bool PAIR, bool ROWB>
 cudaError_t launch_bs(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmC,
                       const BsArgs& a, unsigned grid, cudaStream_t stream) {
     using L = BsLayout<PAIR>;
-    auto kern = fp8_gemm_bs_kernel<PAIR>;
+    auto kern = fp8_gemm_bs_kernel<PAIR, ROWB>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_BYTES);
     if (err != cudaSuccess) return err;
     if constexpr (!PAIR) {
@@ -457,13 +459,10 @@ cudaError_t launch_bs(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUte
     }
 }
 
-}  // namespace
-
-int gemm_bs_tile_n() { return kBN; }
-
-int gemm_bs_pair_max_clusters() {
+template <bool ROWB>
+int bs_pair_max_clusters() {
     using L = BsLayout<true>;
-    if (cudaFuncSetAttribute(fp8_gemm_bs_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(fp8_gemm_bs_kernel<true, ROWB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              L::SMEM_BYTES) != cudaSuccess)
         return 0;
     cudaLaunchConfig_t cfg = {};
@@ -478,14 +477,22 @@ int gemm_bs_pair_max_clusters() {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, fp8_gemm_bs_kernel<true>, &cfg) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveClusters(&n, fp8_gemm_bs_kernel<true, ROWB>, &cfg) != cudaSuccess) return 0;
     return n;
+}
+
+}  // namespace
+
+int gemm_bs_tile_n() { return kBN; }
+
+int gemm_bs_pair_max_clusters(bool row_scaled_b) {
+    return row_scaled_b ? bs_pair_max_clusters<true>() : bs_pair_max_clusters<false>();
 }
 
 cudaError_t launch_gemm_bs(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmC,
                            const uint8_t* sa, const uint8_t* sb, int32_t M, int32_t N, int32_t K,
-                           bool pair, int pair_clusters, uint64_t timeout_ns, uint32_t debug, int num_sms,
-                           cudaStream_t stream) {
+                           bool row_scaled_b, bool pair, int pair_clusters, uint64_t timeout_ns,
+                           uint32_t debug, int num_sms, cudaStream_t stream) {
     BsArgs a;
     a.sa = sa;
     a.sb = sb;
@@ -503,10 +510,13 @@ cudaError_t launch_gemm_bs(const CUtensorMap* tmA, const CUtensorMap* tmB, const
     a.debug = debug;
     if (pair) {
         const int64_t clusters = units < pair_clusters ? units : pair_clusters;
-        return launch_bs<true>(tmA, tmB, tmC, a, static_cast<unsigned>(2 * clusters), stream);
+        const unsigned grid = static_cast<unsigned>(2 * clusters);
+        return row_scaled_b ? launch_bs<true, true>(tmA, tmB, tmC, a, grid, stream)
+                            : launch_bs<true, false>(tmA, tmB, tmC, a, grid, stream);
     }
-    return launch_bs<false>(tmA, tmB, tmC, a, static_cast<unsigned>(units < num_sms ? units : num_sms),
-                            stream);
+    const unsigned grid = static_cast<unsigned>(units < num_sms ? units : num_sms);
+    return row_scaled_b ? launch_bs<false, true>(tmA, tmB, tmC, a, grid, stream)
+                        : launch_bs<false, false>(tmA, tmB, tmC, a, grid, stream);
 }
 
 cudaError_t read_bs_status(uint32_t* out, bool clear) {

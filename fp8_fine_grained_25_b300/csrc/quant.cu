@@ -510,7 +510,8 @@ constexpr int kTThreads = 256;
 struct ActTArgs {
     const uint8_t* x;  // bf16 [M, K]
     uint8_t* qt;       // [K, M]
-    float* st;         // [K, MB]
+    float* st;         // [K, MB] fp32 scales
+    uint8_t* st8;      // [K, MB] UE8M0 scale bytes (POW2)
     int64_t M, K;
     uint32_t MB, KB;
 };
@@ -553,6 +554,7 @@ __device__ __forceinline__ void load_block_t(const ActTArgs& a, uint32_t b, int 
     for (int i = 0; i < 16; ++i) v[i] = live ? __ldg(src + i * pitch) : make_uint2(0u, 0u);
 }
 
+template <bool POW2>  // POW2: UE8M0 scales
 __global__ void __launch_bounds__(kTThreads, 2) quant_act_t_kernel(const ActTArgs a) {
     __shared__ uint32_t red[8][64];  // [warp][column pair]: packed |bf16| maxima
     __shared__ float4 s_sh[32], r_sh[32];
@@ -582,12 +584,18 @@ __global__ void __launch_bounds__(kTThreads, 2) quant_act_t_kernel(const ActTArg
 #pragma unroll
             for (int i = 0; i < 8; ++i) m = __vmaxu2(m, red[i][c >> 1]);
             const float amax = __uint_as_float((c & 1) ? (m & 0xFFFF0000u) : (m << 16));
-            const float sc = tile_scale(amax);
-            const float rc = amax >= kFastDivMinAmax ? __frcp_rn(sc) : 0.0f;
+            float sc, rc;
+            bool fast;
+            uint32_t byte;
+            tile_scale_for<POW2>(amax, sc, rc, fast, byte);
+            if (!fast) rc = 0.0f;  // the IEEE-divide range (fp32 scales only)
             reinterpret_cast<float*>(s_sh)[c] = sc;
             reinterpret_cast<float*>(r_sh)[c] = rc;
             const int64_t col = static_cast<int64_t>(kb) * 128 + c;
-            if (col < a.K) a.st[col * a.MB + mb] = sc;
+            if (col < a.K) {
+                if constexpr (POW2) a.st8[col * a.MB + mb] = static_cast<uint8_t>(byte);
+                else a.st[col * a.MB + mb] = sc;
+            }
         }
         __syncthreads();
         if (live) {
@@ -646,8 +654,10 @@ struct WeightPlainArgs {
     const uint8_t* w;  // bf16 [N, K]
     uint8_t* q;        // [N, K] (WQ)
     float* s;          // [NB, KB] (WQ)
+    uint8_t* s8;       // [NB, KB] UE8M0 bytes (WQ, POW2)
     uint8_t* qt;       // [K, N] (WT)
     float* st;         // [KB, NB] (WT)
+    uint8_t* st8;      // [KB, NB] UE8M0 bytes (WT, POW2)
     int64_t N, K;
     uint32_t NB, KB;
 };
@@ -678,7 +688,7 @@ __device__ __forceinline__ void load_weight_block(const WeightPlainArgs& a, uint
         v[i] = (k < a.K && n0 + i < a.N) ? __ldg(src + i * pitch) : make_uint2(0u, 0u);
 }
 
-template <bool WQ, bool WT>
+template <bool WQ, bool WT, bool POW2>  // POW2: UE8M0 scales
 __global__ void __launch_bounds__(kTThreads, 2) quant_weight_plain_kernel(const WeightPlainArgs a) {
     __shared__ uint32_t red[8];
     __shared__ float2 sr_sh;  // the block's scale and reciprocal (0: IEEE-divide range)
@@ -706,10 +716,18 @@ __global__ void __launch_bounds__(kTThreads, 2) quant_weight_plain_kernel(const 
 #pragma unroll
             for (int i = 1; i < 8; ++i) m = max(m, red[i]);
             const float amax = __uint_as_float(m << 16);
-            const float sc = tile_scale(amax);
-            sr_sh = make_float2(sc, amax >= kFastDivMinAmax ? __frcp_rn(sc) : 0.0f);
-            if constexpr (WQ) a.s[static_cast<uint64_t>(nb) * a.KB + kb] = sc;
-            if constexpr (WT) a.st[static_cast<uint64_t>(kb) * a.NB + nb] = sc;
+            float sc, rc;
+            bool fast;
+            uint32_t byte;
+            tile_scale_for<POW2>(amax, sc, rc, fast, byte);
+            sr_sh = make_float2(sc, fast ? rc : 0.0f);
+            if constexpr (POW2) {
+                if constexpr (WQ) a.s8[static_cast<uint64_t>(nb) * a.KB + kb] = static_cast<uint8_t>(byte);
+                if constexpr (WT) a.st8[static_cast<uint64_t>(kb) * a.NB + nb] = static_cast<uint8_t>(byte);
+            } else {
+                if constexpr (WQ) a.s[static_cast<uint64_t>(nb) * a.KB + kb] = sc;
+                if constexpr (WT) a.st[static_cast<uint64_t>(kb) * a.NB + nb] = sc;
+            }
         }
         __syncthreads();
         const float2 sr = sr_sh;
@@ -859,53 +877,66 @@ cudaError_t launch_quant_weight(const CUtensorMap* tmW, void* q, void* s, bool p
     return cudaGetLastError();
 }
 
-template <bool WQ, bool WT>
+template <bool WQ, bool WT, bool POW2>
 cudaError_t launch_weight_plain(const WeightPlainArgs& a, cudaStream_t stream, int num_sms) {
     int per_sm = 0;
     cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &per_sm, quant_weight_plain_kernel<WQ, WT>, kTThreads, 0);
+        &per_sm, quant_weight_plain_kernel<WQ, WT, POW2>, kTThreads, 0);
     if (err != cudaSuccess) return err;
     const uint64_t nblocks = static_cast<uint64_t>(a.NB) * a.KB;
     const uint64_t cap = static_cast<uint64_t>(num_sms) * (per_sm > 0 ? per_sm : 1);
-    quant_weight_plain_kernel<WQ, WT>
+    quant_weight_plain_kernel<WQ, WT, POW2>
         <<<static_cast<unsigned>(nblocks < cap ? nblocks : cap), kTThreads, 0, stream>>>(a);
     return cudaGetLastError();
 }
 
-cudaError_t launch_quant_weight_t(const void* w, void* q, float* s, void* qt, float* st, int64_t N,
+cudaError_t launch_quant_weight_t(const void* w, void* q, void* s, void* qt, void* st, bool pow2, int64_t N,
                                   int64_t K, cudaStream_t stream, int num_sms) {
     WeightPlainArgs p;
     p.w = static_cast<const uint8_t*>(w);
     p.q = static_cast<uint8_t*>(q);
-    p.s = s;
+    p.s = pow2 ? nullptr : static_cast<float*>(s);
+    p.s8 = pow2 ? static_cast<uint8_t*>(s) : nullptr;
     p.qt = static_cast<uint8_t*>(qt);
-    p.st = st;
+    p.st = pow2 ? nullptr : static_cast<float*>(st);
+    p.st8 = pow2 ? static_cast<uint8_t*>(st) : nullptr;
     p.N = N;
     p.K = K;
     p.NB = static_cast<uint32_t>((N + 127) / 128);
     p.KB = static_cast<uint32_t>((K + 127) / 128);
-    if (q == nullptr) return launch_weight_plain<false, true>(p, stream, num_sms);
-    return launch_weight_plain<true, true>(p, stream, num_sms);
+    if (pow2) {
+        if (q == nullptr) return launch_weight_plain<false, true, true>(p, stream, num_sms);
+        return launch_weight_plain<true, true, true>(p, stream, num_sms);
+    }
+    if (q == nullptr) return launch_weight_plain<false, true, false>(p, stream, num_sms);
+    return launch_weight_plain<true, true, false>(p, stream, num_sms);
 }
 
-cudaError_t launch_quant_act_t(const void* x, void* qt, float* st, int64_t M, int64_t K,
-                               cudaStream_t stream, int num_sms) {
-    ActTArgs a;
-    a.x = static_cast<const uint8_t*>(x);
-    a.qt = static_cast<uint8_t*>(qt);
-    a.st = st;
-    a.M = M;
-    a.K = K;
-    a.MB = static_cast<uint32_t>((M + 127) / 128);
-    a.KB = static_cast<uint32_t>((K + 127) / 128);
+template <bool POW2>
+cudaError_t launch_act_t(const ActTArgs& a, cudaStream_t stream, int num_sms) {
     int per_sm = 0;
-    cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quant_act_t_kernel,
+    cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quant_act_t_kernel<POW2>,
                                                                     kTThreads, 0);
     if (err != cudaSuccess) return err;
     const uint64_t nblocks = static_cast<uint64_t>(a.MB) * a.KB;
     const uint64_t cap = static_cast<uint64_t>(num_sms) * (per_sm > 0 ? per_sm : 1);
-    quant_act_t_kernel<<<static_cast<unsigned>(nblocks < cap ? nblocks : cap), kTThreads, 0, stream>>>(a);
+    quant_act_t_kernel<POW2>
+        <<<static_cast<unsigned>(nblocks < cap ? nblocks : cap), kTThreads, 0, stream>>>(a);
     return cudaGetLastError();
+}
+
+cudaError_t launch_quant_act_t(const void* x, void* qt, void* st, bool pow2, int64_t M, int64_t K,
+                               cudaStream_t stream, int num_sms) {
+    ActTArgs a;
+    a.x = static_cast<const uint8_t*>(x);
+    a.qt = static_cast<uint8_t*>(qt);
+    a.st = pow2 ? nullptr : static_cast<float*>(st);
+    a.st8 = pow2 ? static_cast<uint8_t*>(st) : nullptr;
+    a.M = M;
+    a.K = K;
+    a.MB = static_cast<uint32_t>((M + 127) / 128);
+    a.KB = static_cast<uint32_t>((K + 127) / 128);
+    return pow2 ? launch_act_t<true>(a, stream, num_sms) : launch_act_t<false>(a, stream, num_sms);
 }
 
 cudaError_t read_quant_status(uint32_t* out, bool clear) {

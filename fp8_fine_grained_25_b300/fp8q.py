@@ -30,6 +30,9 @@ lib.fp8q_quant_weight_t.argtypes = [_p, _i64, _i64, _p, _p, _p, _p, _p]
 lib.fp8_block_gemm.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p]
 lib.fp8_wgrad_gemm.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p]
 lib.fp8_block_gemm_ue8m0.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p]
+lib.fp8_wgrad_gemm_ue8m0.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p]
+lib.fp8q_quant_act_t_ue8m0.argtypes = [_p, _i64, _i64, _p, _p, _p]
+lib.fp8q_quant_weight_t_ue8m0.argtypes = [_p, _i64, _i64, _p, _p, _p, _p, _p]
 lib.fp8q_gather_rows.argtypes = [_p, _p, _i64, _i64, _p, _i64, _p, _p, _p]
 lib.fp8q_gather_rows.restype = ctypes.c_int
 lib.fp8_grouped_gemm.argtypes = [_p, _p, _p, _p, _p, _p, _i32, _i64, _i64, _i64, _p]
@@ -46,7 +49,8 @@ lib.fp8q_status_string.argtypes = [ctypes.c_int]
 lib.fp8q_status_string.restype = ctypes.c_char_p
 for _f in ("fp8q_quant_act", "fp8q_quant_weight", "fp8q_quant_act_t", "fp8q_quant_weight_t",
            "fp8q_quant_act_ue8m0", "fp8q_quant_weight_ue8m0",
-           "fp8_block_gemm", "fp8_wgrad_gemm", "fp8_block_gemm_ue8m0", "fp8_grouped_gemm",
+           "fp8_block_gemm", "fp8_wgrad_gemm", "fp8_block_gemm_ue8m0", "fp8_wgrad_gemm_ue8m0",
+           "fp8q_quant_act_t_ue8m0", "fp8q_quant_weight_t_ue8m0", "fp8_grouped_gemm",
            "fp8q_get_device_status"):
     getattr(lib, _f).restype = ctypes.c_int
 
@@ -219,6 +223,50 @@ def fp8q_quant_weight_t(w: torch.Tensor, q: torch.Tensor | None = None,
     return q, scales, qt, st
 
 
+def fp8q_quant_act_t_ue8m0(x: torch.Tensor, qt: torch.Tensor | None = None,
+                           st: torch.Tensor | None = None, stream=None):
+    """128x1 tiles with UE8M0 scales, written transposed -> (qt uint8 [K, M],
+    st uint8 [K, ceil(M/128)])."""
+    M, K = x.shape
+    _need(x, "x", (torch.bfloat16,), None)
+    if qt is None:
+        qt = torch.empty((K, M), dtype=torch.uint8, device=x.device)
+    if st is None:
+        st = torch.empty((K, _cdiv(M, 128)), dtype=torch.uint8, device=x.device)
+    _need(qt, "qt", CODE_DTYPES, (K, M))
+    _need(st, "st", (torch.uint8,), (K, _cdiv(M, 128)))
+    _check(lib.fp8q_quant_act_t_ue8m0(x.data_ptr(), M, K, qt.data_ptr(), st.data_ptr(), _stream(stream)),
+           "fp8q_quant_act_t_ue8m0")
+    return qt, st
+
+
+def fp8q_quant_weight_t_ue8m0(w: torch.Tensor, q: torch.Tensor | None = None,
+                              scales: torch.Tensor | None = None, qt: torch.Tensor | None = None,
+                              st: torch.Tensor | None = None, with_forward: bool = True, stream=None):
+    """128x128 UE8M0 blocks in both layouts -> (q [N, K], s uint8 [NB, KB],
+    qt [K, N], st uint8 [KB, NB]); with_forward=False skips q and s."""
+    _need(w, "w", (torch.bfloat16,), None)
+    N, K = w.shape
+    NB, KB = _cdiv(N, 128), _cdiv(K, 128)
+    dev = w.device
+    if with_forward:
+        q = torch.empty((N, K), dtype=torch.uint8, device=dev) if q is None else q
+        scales = torch.empty((NB, KB), dtype=torch.uint8, device=dev) if scales is None else scales
+        _need(q, "q", CODE_DTYPES, (N, K))
+        _need(scales, "scales", (torch.uint8,), (NB, KB))
+    else:
+        q = scales = None
+    qt = torch.empty((K, N), dtype=torch.uint8, device=dev) if qt is None else qt
+    st = torch.empty((KB, NB), dtype=torch.uint8, device=dev) if st is None else st
+    _need(qt, "qt", CODE_DTYPES, (K, N))
+    _need(st, "st", (torch.uint8,), (KB, NB))
+    _check(lib.fp8q_quant_weight_t_ue8m0(w.data_ptr(), N, K, q.data_ptr() if q is not None else None,
+                                         scales.data_ptr() if scales is not None else None,
+                                         qt.data_ptr(), st.data_ptr(), _stream(stream)),
+           "fp8q_quant_weight_t_ue8m0")
+    return q, scales, qt, st
+
+
 def fp8q_gather_rows(q_src: torch.Tensor, s_src: torch.Tensor, index: torch.Tensor,
                      q_dst: torch.Tensor | None = None, s_dst: torch.Tensor | None = None,
                      stream=None):
@@ -293,6 +341,24 @@ def fp8_block_gemm_ue8m0(A: torch.Tensor, sa: torch.Tensor, B: torch.Tensor, sb:
     _need(C, "C", (torch.bfloat16,), (M, N))
     _check(lib.fp8_block_gemm_ue8m0(A.data_ptr(), sa.data_ptr(), B.data_ptr(), sb.data_ptr(),
                                     C.data_ptr(), M, N, K, _stream(stream)), "fp8_block_gemm_ue8m0")
+    return C
+
+
+def fp8_wgrad_gemm_ue8m0(A: torch.Tensor, sa: torch.Tensor, B: torch.Tensor, sb: torch.Tensor,
+                         C: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """C[M, N] (bf16) = A[M, K] * B[N, K]^T with one UE8M0 byte per row of A
+    and of B per 128-wide K block (sa [M, KB], sb [N, KB])."""
+    M, K = A.shape
+    N = B.shape[0]
+    _need(A, "A", CODE_DTYPES, (M, K))
+    _need(B, "B", CODE_DTYPES, (N, K))
+    _need(sa, "sa", (torch.uint8,), (M, _cdiv(K, 128)))
+    _need(sb, "sb", (torch.uint8,), (N, _cdiv(K, 128)))
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    _need(C, "C", (torch.bfloat16,), (M, N))
+    _check(lib.fp8_wgrad_gemm_ue8m0(A.data_ptr(), sa.data_ptr(), B.data_ptr(), sb.data_ptr(),
+                                    C.data_ptr(), M, N, K, _stream(stream)), "fp8_wgrad_gemm_ue8m0")
     return C
 
 

@@ -170,5 +170,13 @@ def dense_square_ue8m0(seed: int = 0, device="cpu", M: int = 8192) -> Workload:
     return w
 
 
+def dense_backward_ue8m0(seed: int = 0, device="cpu", T: int = 8192) -> Workload:
+    """dense_backward's tensors with power-of-two (UE8M0) scales throughout."""
+    w = dense_backward(seed, device, T)
+    w.name = f"dense backward {T}x7168x7168 (dX and dW), UE8M0 scales"
+    w.scales = "ue8m0"
+    return w
+
+
 CONFIGS = {1: tiny, 2: mla_down, 3: dense_square, 4: moe_grouped, 5: large_m, 6: mla_down_fused,
-           7: moe_dispatch_fp8, 8: dense_backward, 9: dense_square_ue8m0}
+           7: moe_dispatch_fp8, 8: dense_backward, 9: dense_square_ue8m0, 10: dense_backward_ue8m0}

@@ -198,6 +198,28 @@ FP8Q_API int fp8_block_gemm_ue8m0(const void* A, const uint8_t* sa, const void* 
                                   void* C_bf16, int64_t M, int64_t N, int64_t K, cudaStream_t stream);
 
 /*
+ * The UE8M0 forms of the backward pass (see fp8q_quant_act_t,
+ * fp8q_quant_weight_t and fp8_wgrad_gemm for the layouts), with
+ * power-of-two scales stored as UE8M0 bytes:
+ *   fp8q_quant_act_t_ue8m0:    x [M, K] -> qt [K, M], st uint8 [K, ceil(M/128)]
+ *   fp8q_quant_weight_t_ue8m0: w [N, K] -> q, scales (optional, uint8
+ *                              [ceil(N/128), ceil(K/128)]), qt [K, N],
+ *                              st uint8 [ceil(K/128), ceil(N/128)]
+ *   fp8_wgrad_gemm_ue8m0:      C [M, N] = A [M, K] * B [N, K]^T with one
+ *                              UE8M0 byte per row of A and of B per 128-wide
+ *                              K block (sa [M][KB], sb [N][KB]), applied by
+ *                              the tensor core.
+ * Same alignment, error and accuracy rules as the FP32-scale forms, except
+ * that the byte scales need no alignment.
+ */
+FP8Q_API int fp8q_quant_act_t_ue8m0(const void* x_bf16, int64_t M, int64_t K, void* qt_e4m3,
+                                    uint8_t* st, cudaStream_t stream);
+FP8Q_API int fp8q_quant_weight_t_ue8m0(const void* w_bf16, int64_t N, int64_t K, void* q_e4m3,
+                                       uint8_t* scales, void* qt_e4m3, uint8_t* st, cudaStream_t stream);
+FP8Q_API int fp8_wgrad_gemm_ue8m0(const void* A, const uint8_t* sa, const void* B, const uint8_t* sb,
+                                  void* C_bf16, int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+
+/*
  * Grouped (per-expert) block-scaled FP8 GEMM for the MoE FFN (news.qq.com
  * page, "DeepSeekMoE 架构": 256 routed experts, 8 per token). Rows of A are
  * grouped by expert: rows [off[e], off[e+1]) use expert e's weights.

@@ -130,3 +130,49 @@ def test_block_gemm_ue8m0_from_quantizers_full_size(q):
     qbr, sbr = oracle.quant_weight_ue8m0(bits(w.weights["B"]))
     c32, S = oracle.gemm_ue8m0(qar, sar, qbr, sbr, cols=cols)
     assert_gemm_ok(to_f32(C)[np.ix_(rows, cols)], c32, S, "ue8m0 dense 8192x7168x7168")
+
+
+# ---- UE8M0 backward: 128x1 activation tiles, transposed weight blocks,
+# ---- and the row-scaled GEMM with hardware block scaling
+@pytest.mark.parametrize("M,K", [(128, 128), (400, 208), (4096, 576)])
+def test_quant_act_t_ue8m0_matches_oracle(q, M, K):
+    x = workloads.activations_with_outliers(M, K, seed=M + 2 * K, device=DEV)
+    qt, st = q.fp8q_quant_act_t_ue8m0(x)
+    torch.cuda.synchronize()
+    qr, sr = oracle.quant_act_t_ue8m0(bits(x))
+    assert_codes_equal(qt, qr, f"act_t ue8m0 {M}x{K} codes")
+    _bytes_equal(st, sr, f"act_t ue8m0 {M}x{K}")
+
+
+@pytest.mark.parametrize("N,K", [(256, 512), (320, 272)])
+def test_quant_weight_t_ue8m0_matches_oracle(q, N, K):
+    w = workloads.normal_bf16((N, K), 0.02, seed=N + 7 * K, device=DEV)
+    qw, sw, qt, st = q.fp8q_quant_weight_t_ue8m0(w)
+    torch.cuda.synchronize()
+    q_r, s_r, qt_r, st_r = oracle.quant_weight_t_ue8m0(bits(w))
+    assert_codes_equal(qw, q_r, f"weight_t ue8m0 {N}x{K} forward codes")
+    _bytes_equal(sw, s_r, f"weight_t ue8m0 {N}x{K} forward")
+    assert_codes_equal(qt, qt_r, f"weight_t ue8m0 {N}x{K} transposed codes")
+    _bytes_equal(st, st_r, f"weight_t ue8m0 {N}x{K} transposed")
+
+
+@pytest.mark.parametrize("pairs", [True, False])
+@pytest.mark.parametrize("M,N,K", [(256, 224, 512), (300, 520, 400), (384, 448, 2048)])
+def test_wgrad_gemm_ue8m0_random_codes(q, M, N, K, pairs):
+    from gpu_helpers import assert_gemm_ok, to_f32
+    rng = np.random.default_rng(M * 5 + N + K)
+    KB = -(-K // 128)
+    qa = rng.choice(FINITE, size=(M, K)).astype(np.uint8)
+    qb = rng.choice(FINITE, size=(N, K)).astype(np.uint8)
+    sa = rng.integers(110, 140, size=(M, KB)).astype(np.uint8)
+    sb = rng.integers(110, 140, size=(N, KB)).astype(np.uint8)
+    t = lambda a: torch.from_numpy(a).to(DEV)
+    q.fp8q_set_gemm_pairs(pairs)
+    try:
+        C = q.fp8_wgrad_gemm_ue8m0(t(qa), t(sa), t(qb), t(sb))
+        torch.cuda.synchronize()
+    finally:
+        q.fp8q_set_gemm_pairs(True)
+    c32, S = oracle.wgrad_gemm_ue8m0(qa, sa, qb, sb)
+    assert_gemm_ok(to_f32(C), c32, S, f"wgrad ue8m0 {M}x{N}x{K} pairs={pairs}")
+    assert q.fp8q_get_device_status() == 0
