@@ -149,7 +149,7 @@ def job_throughput(world: int, flops_per_step: float, steps: int, seconds: float
 # ---------------------------------------------------------------- workloads
 def make_workload(config: int, device):
     from fp8_fine_grained_25_b300 import workloads
-    return workloads.CONFIGS[config](seed=0, device=device)
+    return workloads.WORKLOADS[config](seed=0, device=device)
 
 
 def step_flops(w) -> float:

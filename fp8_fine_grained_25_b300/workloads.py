@@ -178,5 +178,5 @@ def dense_backward_ue8m0(seed: int = 0, device="cpu", T: int = 8192) -> Workload
     return w
 
 
-CONFIGS = {1: tiny, 2: mla_down, 3: dense_square, 4: moe_grouped, 5: large_m, 6: mla_down_fused,
+WORKLOADS = {1: tiny, 2: mla_down, 3: dense_square, 4: moe_grouped, 5: large_m, 6: mla_down_fused,
            7: moe_dispatch_fp8, 8: dense_backward, 9: dense_square_ue8m0, 10: dense_backward_ue8m0}

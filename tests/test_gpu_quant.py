@@ -74,7 +74,7 @@ def test_quant_does_not_write_outside_outputs(q):
 @pytest.mark.parametrize("cfg", [1, 2, 3, 5])
 def test_quant_act_full_size(q, cfg):
     from fp8_fine_grained_25_b300 import workloads
-    w = workloads.CONFIGS[cfg](seed=0, device=DEV)
+    w = workloads.WORKLOADS[cfg](seed=0, device=DEV)
     qg, sg = q.fp8q_quant_act(w.A)
     qo, so = oracle.quant_act(bits(w.A))
     assert_scales_equal(sg, so, f"config {cfg} act scales")
