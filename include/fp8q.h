@@ -265,6 +265,11 @@ FP8Q_API int fp8_wgrad_gemm(const void* A, const float* sa, const void* B, const
 FP8Q_API int fp8q_get_device_status(cudaStream_t stream, uint32_t* status_out, int clear);
 
 /*
+ * The fp8q_set_* calls below change process-wide settings that later calls
+ * read when they launch; they are meant for tests and tuning, are not
+ * synchronised with calls made concurrently from other host threads, and do
+ * not affect work already enqueued.
+ *
  * Time limit for every pipeline wait inside the GEMM kernels, in
  * nanoseconds (default 1e9). A wait that exceeds it sets
  * FP8Q_DEVSTATUS_TIMEOUT, and the kernel drains its in-flight copies,
