@@ -378,7 +378,7 @@ def make_path(w, device):
 
 
 # --------------------------------------------------------------- CPU oracle
-def oracle_sample(w, rows_a: int, rows_b: int, out_rows: int, threads: int):
+def oracle_sample(w, rows_a: int, out_rows: int, threads: int):
     """Time the CPU oracle on a bounded sample of one step and extrapolate
     the full step: quantizer time scales with elements, GEMM time with
     output elements. Returns (seconds for a full step, description)."""
@@ -390,7 +390,6 @@ def oracle_sample(w, rows_a: int, rows_b: int, out_rows: int, threads: int):
     N = Wd.shape[0]
     bits = lambda t: t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
     a_s = bits(A[:rows_a])
-    b_s = bits(Wd[:rows_b])
     pow2 = w.scales == "ue8m0"
     qact = oracle.quant_act_ue8m0 if pow2 else oracle.quant_act
     qweight = oracle.quant_weight_ue8m0 if pow2 else oracle.quant_weight
@@ -457,11 +456,13 @@ def sample_oracle(w, small: bool, threads: int):
     """The bounded oracle sample of one step of workload w (small: the
     reference arm's per-step sample)."""
     if w.X is not None:
-        return oracle_sample_backward(w, rows=64 if small else 256, cols=128,
-                                      out_rows=4 if small else 32, threads=threads)
+        if small:
+            return oracle_sample_backward(w, rows=64, cols=128, out_rows=4, threads=threads)
+        return oracle_sample_backward(w, rows=4096, cols=2048, out_rows=1536, threads=threads)
     if small:
-        return oracle_sample(w, rows_a=64, rows_b=128, out_rows=4, threads=threads)
-    return oracle_sample(w, rows_a=256, rows_b=128, out_rows=128, threads=threads)
+        return oracle_sample(w, rows_a=64, out_rows=4, threads=threads)
+    # about 10-30 s of oracle work on an 8- to 16-core host
+    return oracle_sample(w, rows_a=4096, out_rows=3072, threads=threads)
 
 
 def run_reference(args, rank, world):
