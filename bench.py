@@ -54,15 +54,42 @@ def load_peaks():
         return dict(FALLBACK), "fallback"
 
 
+def code_hash(path: str) -> str:
+    """First 16 hex digits of the sha256 of a C/C++/CUDA source with its
+    comments and all whitespace removed, so that editing a comment does not
+    unlink a profile taken on the same code."""
+    with open(path) as fh:
+        src = fh.read()
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c == '"' or c == "'":  # string or character literal, kept whole
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    code = "".join("".join(out).split())
+    return hashlib.sha256(code.encode()).hexdigest()[:16]
+
+
 def profiled_traffic(profile: str, source: str):
     """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum)
     recorded in profiles/<profile> by an ncu capture, or None when the
-    kernel source changed since (its recorded sha256 prefix differs)."""
+    kernel code changed since (its recorded code hash differs)."""
     try:
         with open(os.path.join(ROOT, "profiles", profile)) as fh:
             text = fh.read()
-        with open(os.path.join(ROOT, "fp8_fine_grained_25_b300", "csrc", source), "rb") as fh:
-            cur = hashlib.sha256(fh.read()).hexdigest()[:16]
+        cur = code_hash(os.path.join(ROOT, "fp8_fine_grained_25_b300", "csrc", source))
     except OSError:
         return None
     m = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)

@@ -201,8 +201,12 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 // tiles is one contiguous byte range: a chunk of kActChunkTiles tiles is one
 // bulk copy. Four lanes encode one tile (8 tiles per warp): lane `sub` of
 // the group owns the 16-byte chunks (4j + sub + 8 * (group & 1)) mod 16,
-// j = 0..3, of the tile's 256 bytes; the rotation by 8 chunks for odd groups
-// keeps every 8-lane shared-memory phase on distinct banks.
+// j = 0..3, of the tile's 256 bytes. A 16-byte shared load is served 8
+// lanes (two tiles 256 bytes apart) per pass, and with this rotation the two
+// tiles' chunks share banks: ncu counts 2 wavefronts per pass where 1 would
+// do. A rotation by 4 removes the conflicts but measured no faster (equal at
+// 8192 x 7168, 3 % slower at 32768 x 7168): the kernel is bound by HBM, not
+// by shared memory.
 constexpr int kActConsumerWarps = 16;
 constexpr int kActChunkTiles = 8 * kActConsumerWarps;  // 128 tiles, 32 KB of bf16 at most
 constexpr int kActStages = 4;
