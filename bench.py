@@ -251,14 +251,18 @@ class Path:
     def outputs(self):
         return {n: self.bufs[n][2] for n in self.w.weights}
 
-    def step(self, inp=None, outs=None, events=None, stream=None):
-        """One pass of the path on `stream` (default: the current one)."""
+    def step(self, inp=None, outs=None, events=None, stream=None, only=None):
+        """One pass of the path on `stream` (default: the current one);
+        `only` names the one kernel of `names` to launch by itself."""
         f = self.fp8q
         inp = self.inputs() if inp is None else inp
         A = inp["A"]
         rec = (lambda i: events[i].record(stream)) if events is not None else (lambda i: None)
+        run = lambda name: only is None or only == name
         rec(0)
-        if self.dispatch:
+        if not run("quant_act"):
+            pass
+        elif self.dispatch:
             f.fp8q_quant_act(A, self.qx, self.sx, stream=stream)
             f.fp8q_gather_rows(self.qx, self.sx, self.w.index, self.qa, self.sa, stream=stream)
         elif self.ue8m0:
@@ -269,7 +273,9 @@ class Path:
         i = 2
         for name in self.w.weights:
             qb, sb, _ = self.bufs[name]
-            if self.ue8m0:
+            if not run(f"quant_weight[{name}]"):
+                pass
+            elif self.ue8m0:
                 f.fp8q_quant_weight_ue8m0(inp[name], qb, sb, stream=stream)
             else:
                 f.fp8q_quant_weight(inp[name], qb, sb, stream=stream)
@@ -279,7 +285,9 @@ class Path:
             qb, sb, C = self.bufs[name]
             if outs is not None:
                 C = outs[name]
-            if self.w.offsets is not None:
+            if not run(f"gemm[{name}]"):
+                pass
+            elif self.w.offsets is not None:
                 f.fp8_grouped_gemm(self.qa, self.sa, qb, sb, self.w.offsets, C, stream=stream)
             elif self.ue8m0:
                 f.fp8_block_gemm_ue8m0(self.qa, self.sa, qb, sb, C, stream=stream)
@@ -354,28 +362,35 @@ class BackwardPath:
     def outputs(self):
         return {"dX": self.dX, "dW": self.dW}
 
-    def step(self, inp=None, outs=None, events=None, stream=None):
+    def step(self, inp=None, outs=None, events=None, stream=None, only=None):
         f = self.fp8q
         inp = self.inputs() if inp is None else inp
         outs = self.outputs() if outs is None else outs
         rec = (lambda i: events[i].record(stream)) if events is not None else (lambda i: None)
+        run = lambda name: only is None or only == name
         rec(0)
         u = self.ue8m0
-        (f.fp8q_quant_act_ue8m0 if u else f.fp8q_quant_act)(inp["dY"], self.qdy, self.sdy, stream=stream)
+        if run("quant_act[dY]"):
+            (f.fp8q_quant_act_ue8m0 if u else f.fp8q_quant_act)(inp["dY"], self.qdy, self.sdy, stream=stream)
         rec(1)
-        (f.fp8q_quant_weight_t_ue8m0 if u else f.fp8q_quant_weight_t)(
-            inp["W"], qt=self.qwt, st=self.swt, with_forward=False, stream=stream)
+        if run("quant_weight_t[W]"):
+            (f.fp8q_quant_weight_t_ue8m0 if u else f.fp8q_quant_weight_t)(
+                inp["W"], qt=self.qwt, st=self.swt, with_forward=False, stream=stream)
         rec(2)
-        (f.fp8_block_gemm_ue8m0 if u else f.fp8_block_gemm)(self.qdy, self.sdy, self.qwt, self.swt,
-                                                            outs["dX"], stream=stream)
+        if run("gemm[dX]"):
+            (f.fp8_block_gemm_ue8m0 if u else f.fp8_block_gemm)(self.qdy, self.sdy, self.qwt, self.swt,
+                                                                outs["dX"], stream=stream)
         rec(3)
         act_t = f.fp8q_quant_act_t_ue8m0 if u else f.fp8q_quant_act_t
-        act_t(inp["dY"], self.qdyt, self.sdyt, stream=stream)
+        if run("quant_act_t[dY]"):
+            act_t(inp["dY"], self.qdyt, self.sdyt, stream=stream)
         rec(4)
-        act_t(inp["X"], self.qxt, self.sxt, stream=stream)
+        if run("quant_act_t[X]"):
+            act_t(inp["X"], self.qxt, self.sxt, stream=stream)
         rec(5)
-        (f.fp8_wgrad_gemm_ue8m0 if u else f.fp8_wgrad_gemm)(self.qdyt, self.sdyt, self.qxt, self.sxt,
-                                                            outs["dW"], stream=stream)
+        if run("gemm[dW]"):
+            (f.fp8_wgrad_gemm_ue8m0 if u else f.fp8_wgrad_gemm)(self.qdyt, self.sdyt, self.qxt, self.sxt,
+                                                                outs["dW"], stream=stream)
         rec(6)
 
     def kernels(self, per):
@@ -402,6 +417,32 @@ class BackwardPath:
 
 def make_path(w, device):
     return BackwardPath(w, device) if w.X is not None else Path(w, device)
+
+
+def time_alone(path, names, device, reps: int = 25):
+    """Mean seconds of each named kernel launched by itself, with a 256 MB
+    read just before it so that the L2 holds no dirty lines (inside the step
+    a quantizer also writes back the previous kernel's output) and none of
+    its input. CUDA event timestamps on the B300 advance in steps of
+    2.048 us, so one launch of ~30 us is timed to +-7 %; the mean over `reps`
+    launches averages that out (a median would stay on the 2.048 us grid)."""
+    clean = torch.ones(256 << 20, dtype=torch.uint8, device=device)
+    out = {}
+    for n in names:
+        for _ in range(3):
+            path.step(only=n)
+        ts = []
+        for _ in range(reps):
+            clean.sum()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            path.step(only=n)
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) / 1e3)
+        out[n] = statistics.fmean(ts)
+    del clean
+    return out
 
 
 # --------------------------------------------------------------- CPU oracle
@@ -583,6 +624,15 @@ def main():
     for v in kern.values():
         if "GB/s" in v:
             v["frac_hbm"] = v["GB/s"] / peaks["hbm_gbs"]
+    # the quantizers again, each launched alone (after the timed region)
+    quant_names = [n for n in path.names if n not in path.gemm_names]
+    alone = time_alone(path, quant_names, device)
+    kern_alone = path.kernels({n: alone.get(n, per[n]) for n in path.names})
+    for n in quant_names:
+        k = n if n in kern else next(k for k in kern if k.startswith(n))  # quant_act+dispatch
+        kern[k]["alone_ms"] = alone[n] * 1e3
+        kern[k]["alone_GB/s"] = kern_alone[k]["GB/s"]
+        kern[k]["alone_frac_hbm"] = kern_alone[k]["GB/s"] / peaks["hbm_gbs"]
 
     # dominant kernel: the GEMM(s) (the weight-gradient GEMM in the backward
     # step). It runs inside a long back-to-back loop (power-capped), so the
