@@ -23,9 +23,9 @@ struct DeviceInfo {
     bool supported = false;
     int sms = 0;
     // co-resident 2-CTA clusters of the pair kernel, per tile width
-    // ([0]: 128, [1]: 256) and B-scale layout ([0]: 128x128 blocks, [1]: one
-    // per row); -1: not queried yet
-    int pair_clusters[2][2] = {{-1, -1}, {-1, -1}};
+    // ([0]: 128, [1]: 256, [2]: 224) and B-scale layout ([0]: 128x128 blocks,
+    // [1]: one per row); -1: not queried yet
+    int pair_clusters[3][2] = {{-1, -1}, {-1, -1}, {-1, -1}};
     int bs_pair_clusters[2] = {-1, -1};  // the same for the UE8M0 (hardware-scaled) GEMM
 };
 
@@ -96,12 +96,19 @@ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // Output-tile width: the one with the fewest tile-width units of work per
 // SM after rounding up to whole waves (a tile of width BN costs BN + 64
 // units: the fixed part is the 128-row A traffic and the per-tile epilogue).
-int choose_bn(int64_t M, int64_t N, int sms) {
+// Output-tile width by a wave model: waves of tiles over the SMs times the
+// tile's cost, its width plus a fixed share for the per-K-block handshake
+// that does not shrink with the width. The shares reproduce measured
+// per-column costs relative to 256: 1.2 for 128 and 1.05 for 224. 224
+// (block-scaled B only) fills whole waves more often at 7168-wide outputs
+// and wastes fewer columns at N = 576; ties keep the earlier candidate.
+int choose_bn(int64_t M, int64_t N, int sms, bool allow224) {
     int best = 256;
     int64_t best_cost = -1;
-    for (int bn : {256, 128}) {
+    for (int bn : {256, 128, 224}) {
+        if (bn == 224 && !allow224) continue;
         const int64_t tiles = cdiv(M, 128) * cdiv(N, bn);
-        const int64_t cost = cdiv(tiles, sms) * (bn + 64);
+        const int64_t cost = cdiv(tiles, sms) * (bn + (bn == 224 ? 70 : 64));
         if (best_cost < 0 || cost < best_cost) {
             best = bn;
             best_cost = cost;
@@ -132,7 +139,7 @@ const char* fp8q_status_string(int status) {
 void fp8q_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns = ns ? ns : 1000000000ull; }
 
 int fp8q_set_gemm_tile_n(int bn) {
-    if (bn != 0 && bn != 128 && bn != 256) return FP8Q_ERR_UNSUPPORTED;
+    if (bn != 0 && bn != 128 && bn != 224 && bn != 256) return FP8Q_ERR_UNSUPPORTED;
     g_force_bn = bn;
     return FP8Q_OK;
 }
@@ -320,11 +327,14 @@ int dense_gemm(const void* A, const float* sa, const void* B, const float* sb, v
     DeviceInfo* dev = nullptr;
     if (int rc = current_device(&dev)) return rc;
 
-    const int bn = g_force_bn ? g_force_bn : choose_bn(M, N, dev->sms);
-    // 2-CTA pairs (256 x 256 tiles over two SMs) for the 256-wide tile when
-    // there are at least two m-tiles to pair.
+    // the 224-wide tile exists for block-scaled B only; a forced 224 runs the
+    // row-scaled GEMM 256 wide
+    int bn = g_force_bn ? g_force_bn : choose_bn(M, N, dev->sms, !row_scaled_b);
+    if (bn == 224 && row_scaled_b) bn = 256;
+    // 2-CTA pairs (256-row tiles over two SMs) when there are at least two
+    // m-tiles to pair.
     bool pair = g_pair_mode && M > 128;
-    int* pc = &dev->pair_clusters[bn == 256 ? 1 : 0][row_scaled_b ? 1 : 0];
+    int* pc = &dev->pair_clusters[bn == 256 ? 1 : bn == 224 ? 2 : 0][row_scaled_b ? 1 : 0];
     if (pair) {
         std::lock_guard<std::mutex> lock(g_mutex);
         if (*pc < 0) *pc = fp8q::gemm_pair_max_clusters(bn, row_scaled_b);
@@ -332,9 +342,11 @@ int dense_gemm(const void* A, const float* sa, const void* B, const float* sb, v
     }
     CUtensorMap tmA, tmB, tmC;
     if (!make_map_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, K, M, 128, 128) ||
-        !make_map_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, K, N, 128, pair ? bn / 2 : bn) ||
-        !make_map_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C_bf16, N, M, 32, 32,
-                     CU_TENSOR_MAP_SWIZZLE_64B))
+        !make_map_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, K, N, 128, pair ? bn / 2 : bn))
+        return FP8Q_ERR_CUDA;
+    const int cbox = fp8q::gemm_c_box_cols(bn);  // 32 (64-byte swizzle) or 16 (32-byte)
+    if (!make_map_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C_bf16, N, M, cbox, 32,
+                     cbox == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B))
         return FP8Q_ERR_CUDA;
 
     fp8q::GemmLaunch g{};

@@ -4,7 +4,8 @@
 // "FP8 低精度训练": "细粒度量化" Fig. 7a for the scale granularity,
 // "提高累加精度" Fig. 7b for the promotion into FP32 registers).
 //
-// Per CTA (persistent, one 128 x BN output tile at a time, 12 warps):
+// Per CTA (persistent, one 128 x BN output tile at a time, BN = 128, 224 or
+// 256, 12 warps):
 //   warp 0      TMA producer: per K block, a 128x128 A box and a BNx128 B box
 //               (E4M3, 128-byte swizzle) into a ring of shared-memory stages.
 //   warp 1      MMA issuer: 4 x tcgen05.mma kind::f8f6f4 (K = 32 each) write
@@ -62,24 +63,28 @@ constexpr int kSmemLimit = 232448;
 constexpr int kCtrlRegs = 40, kEpiRegs = 232;  // setmaxnreg split: 128*40 + 256*232 = 384*168
 constexpr int kScaleKb = 4;     // K blocks of scales per ring slot
 constexpr int kScaleSlots = 4;  // ring slots (16 K blocks staged ahead)
-constexpr int kMaxNb = 2;       // 128-column blocks of one tile (BN <= 256, n0 % BN == 0)
 
 // ROWB: B carries one scale per row (1x128 tiles, the weight-gradient GEMM)
 // instead of one per 128x128 block.
 template <int BN, bool GROUPED, bool PAIR, bool ROWB = false>
 struct Layout {
     static constexpr int A_BYTES = BM * BK;
+    // 128-column scale blocks one tile can touch: n0 = BN * t is 128-aligned
+    // for BN = 128 and 256; a 224-wide tile can start inside a block
+    static constexpr int MAX_NB = BN % 128 == 0 ? BN / 128 : BN / 128 + 2;
     static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // rows of B this CTA loads
     static constexpr int B_BYTES = B_ROWS * BK;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    // two 32 rows x 32 bf16 staging boxes per warp (64-byte swizzle): one is
-    // filled while the TMA store of the other is still reading
-    static constexpr int EPI_BOX_BYTES = 32 * 32 * 2;
+    // two 32-row staging boxes per warp, 32 bf16 wide (64-byte swizzle), or
+    // 16 wide (32-byte swizzle) when a warp's columns are not a multiple of
+    // 32: one is filled while the TMA store of the other is still reading
+    static constexpr int EPI_BOX_COLS = (BN / 2) % 32 == 0 ? 32 : 16;
+    static constexpr int EPI_BOX_BYTES = 32 * EPI_BOX_COLS * 2;
     static constexpr int EPI_WARP_BYTES = 2 * EPI_BOX_BYTES;
     static constexpr int EPI_BYTES = GROUPED ? 0 : kEpiWarps * EPI_WARP_BYTES;
-    // slot: sa as [128 rows][kScaleKb], then sb as [kMaxNb][kScaleKb]
+    // slot: sa as [128 rows][kScaleKb], then sb as [MAX_NB][kScaleKb]
     // (ROWB: sb as [kScaleKb][BN], the tile's columns contiguous per K block)
-    static constexpr int SB_PER_KB = ROWB ? BN : kMaxNb;
+    static constexpr int SB_PER_KB = ROWB ? BN : MAX_NB;
     static constexpr int SCALE_SLOT_BYTES = 4 * kScaleKb * (BM + SB_PER_KB);
     static constexpr int SCALE_BYTES = kScaleSlots * SCALE_SLOT_BYTES;
     static constexpr int NBUF = (512 / BN) > 4 ? 4 : (512 / BN);  // TMEM buffers of BN columns
@@ -101,7 +106,11 @@ struct Layout {
     static constexpr int TABLE_OFF = MISC_OFF + 16;
     static constexpr int HALF = BN / 2;       // columns per promotion warp
     static constexpr int CHUNKS = HALF / 32;  // 32-column TMEM loads, issued in pairs
-    static_assert(BN == 128 || BN == 256, "tile width must be 128 or 256");
+    static_assert(BN == 128 || BN == 224 || BN == 256, "tile width must be 128, 224 or 256");
+    static_assert(BN != 224 || (!GROUPED && !ROWB), "224-wide tiles are for the block-scaled dense GEMM");
+    static_assert(BN == 224 || CHUNKS % 2 == 0, "32-column TMEM chunks are loaded in pairs");
+    static_assert((B_ROWS * BK) % 1024 == 0 && STAGE_BYTES % 1024 == 0,
+                  "stages and their B tiles must start on 1024-byte swizzle atoms");
     static_assert(!(PAIR && GROUPED), "pair mode is for the dense GEMM");
     static_assert(!(ROWB && GROUPED), "row-scaled B is for the dense GEMM");
     static_assert(STAGES >= 2, "not enough shared memory for two stages");
@@ -205,6 +214,37 @@ template <bool CLUSTER = false>
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           uint64_t limit) {
     return __all_sync(0xFFFFFFFFu, mbar_wait<CLUSTER>(bar, parity, abort_flag, limit));
+}
+
+// acc[O .. O + NCOL) += P * c, packed.
+template <int O, int NCOL>
+__device__ __forceinline__ void fma_cols(float (&acc)[112], const uint32_t* r, float c) {
+#pragma unroll
+    for (int i = 0; i < NCOL; i += 2) ffma2(acc[O + i], acc[O + i + 1], r[i], r[i + 1], c);
+}
+
+// Promotion of one warp's 112 columns of a 224-wide tile, the same code for
+// both warpgroups (h): 32-column chunks at warp columns b, b + 32, b + 64
+// (b = 16 h) into acc[0, 96), and a 16-column chunk at column 96 - 96 h into
+// acc[96, 112). Every 32-column chunk then starts on a multiple of 32 (the
+// tile starts on one; a warpgroup's 112 columns leave 16 over), so none
+// crosses a 128-column scale block: a chunk at warp column o uses cs when
+// o < split, else csn. Two TMEM loads per wait.
+__device__ __forceinline__ void promote_112(float (&acc)[112], uint32_t taddr, int h, float cs,
+                                            float csn, int split) {
+    const int b = 16 * h, o16 = 96 - 96 * h;
+    uint32_t r0[32], r1[32];
+    tmem_ld32(taddr + b, r0);
+    tmem_ld32(taddr + b + 32, r1);
+    tmem_wait_ld64(r0, r1);
+    fma_cols<0, 32>(acc, r0, b < split ? cs : csn);
+    fma_cols<32, 32>(acc, r1, b + 32 < split ? cs : csn);
+    uint32_t r2[32], r3[16];
+    tmem_ld32(taddr + b + 64, r2);
+    tmem_ld16(taddr + o16, r3);
+    tmem_wait_ld48(r2, r3);
+    fma_cols<64, 32>(acc, r2, b + 64 < split ? cs : csn);
+    fma_cols<96, 16>(acc, r3, o16 < split ? cs : csn);
 }
 
 template <int BN, bool GROUPED, bool PAIR, bool ROWB>
@@ -389,8 +429,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if (warp == kScaleWarp) {
             // ------------------------------------------------- scale loader
             // Slot j holds K blocks [kb0, kb0 + 4): sa of the tile's 128 rows
-            // (row r at floats 4r .. 4r + 3) and sb of the tile's two 128-column
-            // blocks (block i at floats 512 + 4i ..). Rows outside the tile,
+            // (row r at floats 4r .. 4r + 3) and sb of the 128-column blocks the
+            // tile touches (block i at floats 512 + 4i ..). Rows outside the tile,
             // blocks past the last one and K blocks past the end are zero.
             // When KB % 4 == 0 (and sa, sb are 16-byte aligned) each row's four
             // values are one 16-byte copy.
@@ -403,8 +443,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = unit0; ok && t < num_tiles; t += unit_step) {
                 const Tile tile = decode_tile<BN, GROUPED, PAIR>(args, table, t, rank);
                 const float* sb_e = args.sb + static_cast<int64_t>(tile.e) * args.NB * KB;
-                const int nb = (tile.n0 >> 7) + (lane & (kMaxNb - 1));
-                const bool sb_ok = lane < kMaxNb && nb < args.NB && (nb << 7) < tile.n0 + BN;
+                const int nb = (tile.n0 >> 7) + (lane < L::MAX_NB ? lane : 0);
+                const bool sb_ok = lane < L::MAX_NB && nb < args.NB && (nb << 7) < tile.n0 + BN;
                 for (int kb0 = 0; kb0 < KB; kb0 += kScaleKb) {
                     if (!warp_wait(bar(L::SEMPTY + slot), sphase ^ 1u, abort_flag, limit)) {
                         ok = false;
@@ -442,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 cp_async_4(sbl + 4u * (j * BN + c), in ? src + j : args.sb, in ? 4u : 0u);
                             }
                         }
-                    } else if (lane < kMaxNb) {
+                    } else if (lane < L::MAX_NB) {
                         const float* src = sb_e + (sb_ok ? static_cast<int64_t>(nb) * KB + kb0 : 0);
                         const uint32_t dst = sl + 16u * (BM + lane);
                         if (wide) {
@@ -488,10 +528,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < L::HALF; ++j) acc[j] = 0.0f;
 
-            // This warp's columns lie in one 128-column block (n0 % BN == 0),
-            // so each K block needs one scale product sa[m][kb] * sb[nb][kb].
-            const int rel_nb = (h * L::HALF) >> 7;
-            float4 sa4 = make_float4(0.f, 0.f, 0.f, 0.f), sb4 = sa4;
+            // For BN = 128 and 256 this warp's columns lie in one 128-column
+            // block (n0 % BN == 0), so each K block needs one scale product
+            // sa[m][kb] * sb[nb][kb]. A 224-wide tile starts at a multiple of 32
+            // and a warp's 112 columns touch at most two blocks: the first
+            // `split` columns use block rel_nb, the rest block rel_nb + 1.
+            const int wcol = (tile.n0 & 127) + h * L::HALF;  // from the tile's first block
+            const int rel_nb = wcol >> 7;
+            const int split = 128 - (wcol & 127);
+            float4 sa4 = make_float4(0.f, 0.f, 0.f, 0.f), sb4 = sa4, sb4n = sa4;
             const float* sb_cols = scale_ring;  // ROWB: this warp's sb columns in the slot
             for (int kb = 0; kb < KB; ++kb) {
                 const int j = kb & (kScaleKb - 1);
@@ -509,6 +554,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         sb_cols = sl + kScaleKb * BM + h * L::HALF;
                     } else {
                         sb4 = *reinterpret_cast<const float4*>(sl + 4 * (BM + rel_nb));
+                        if constexpr (BN == 224)
+                            sb4n = *reinterpret_cast<const float4*>(sl + 4 * (BM + rel_nb + 1));
                         __syncwarp();
                         if (lane == 0) mbar_arrive(bar(L::SEMPTY + slot));
                         if (++slot == kScaleSlots) {
@@ -520,6 +567,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float a_s = j == 0 ? sa4.x : j == 1 ? sa4.y : j == 2 ? sa4.z : sa4.w;
                 const float b_s = j == 0 ? sb4.x : j == 1 ? sb4.y : j == 2 ? sb4.z : sb4.w;
                 const float cs = a_s * b_s;
+                const float b_sn = j == 0 ? sb4n.x : j == 1 ? sb4n.y : j == 2 ? sb4n.z : sb4n.w;
+                const float csn = a_s * b_sn;  // BN = 224: the warp's second block
 
                 if (!warp_wait<PAIR>(bar(L::TFULL + abuf), aphase, abort_flag, limit)) {
                     ok = false;
@@ -547,6 +596,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ffma2_cols(a[2], a[3], r0[4 * i + 2], r0[4 * i + 3], a_s, b[i].z, b[i].w);
                         }
                     }
+                } else if constexpr (BN == 224) {
+                    promote_112(acc, taddr, h, cs, csn, split);
                 } else {
 #pragma unroll
                     for (int c = 0; c < L::CHUNKS; c += 2) {
@@ -585,31 +636,39 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
 
             if constexpr (!GROUPED) {
-                // bf16 -> 64-byte-swizzled staging (32 rows x 64 B per box,
-                // two boxes per warp) -> TMA store, 32 columns at a time
+                // bf16 -> swizzled staging (32 rows x EPI_BOX_COLS per box, two
+                // boxes per warp) -> TMA store, one box at a time. Row r of a
+                // box holds EPI_BOX_COLS / 8 16-byte pieces; piece j sits at
+                // j ^ (r / 2 % 4) for the 64-byte swizzle (32 columns) and at
+                // j ^ (r / 4 % 2) for the 32-byte swizzle (16 columns). Box c2
+                // stores acc[BC c2, +BC); for BN = 224 those are warp columns
+                // 16 h + 16 c2 for c2 < 6 and 96 - 96 h for c2 = 6 (the
+                // promotion's chunk order).
+                constexpr int BC = L::EPI_BOX_COLS;
                 uint8_t* ebuf0 = smem + L::EPI_OFF + ew * L::EPI_WARP_BYTES;
                 const uint32_t ebuf0_s = sbase + L::EPI_OFF + ew * L::EPI_WARP_BYTES;
 #pragma unroll
-                for (int c2 = 0; c2 < L::HALF / 32; ++c2) {
+                for (int c2 = 0; c2 < L::HALF / BC; ++c2) {
                     uint8_t* ebuf = ebuf0 + (c2 & 1) * L::EPI_BOX_BYTES;
                     const uint32_t ebuf_s = ebuf0_s + (c2 & 1) * L::EPI_BOX_BYTES;
                     // the store issued two boxes ago (same buffer) must have read it
                     if (lane == 0) bulk_wait_group_read1();
                     __syncwarp();
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const float* v = acc + 32 * c2 + 8 * j;
+                    for (int j = 0; j < BC / 8; ++j) {
+                        const float* v = acc + BC * c2 + 8 * j;
                         uint4 pk;
                         pk.x = pack_bf16x2(v[0], v[1]);
                         pk.y = pack_bf16x2(v[2], v[3]);
                         pk.z = pack_bf16x2(v[4], v[5]);
                         pk.w = pack_bf16x2(v[6], v[7]);
-                        const int phys = j ^ ((lane >> 1) & 3);
-                        *reinterpret_cast<uint4*>(ebuf + lane * 64 + phys * 16) = pk;
+                        const int phys = BC == 32 ? j ^ ((lane >> 1) & 3) : j ^ ((lane >> 2) & 1);
+                        *reinterpret_cast<uint4*>(ebuf + lane * (2 * BC) + phys * 16) = pk;
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
-                    const int x = col0 + 32 * c2, y = tile.m0 + quarter * 32;
+                    const int wc = BN != 224 ? BC * c2 : c2 < 6 ? 16 * h + 16 * c2 : 96 - 96 * h;
+                    const int x = col0 + wc, y = tile.m0 + quarter * 32;
                     if (lane == 0 && x < args.N && y < args.M) {
                         tma_store_2d(&tmC, ebuf_s, x, y);
                         bulk_commit_group();
@@ -719,7 +778,17 @@ int pair_max_clusters() {
 int gemm_stages(int bn) {
     switch (bn) {
         case 128: return Layout<128, false, false>::STAGES;
+        case 224: return Layout<224, false, false>::STAGES;
         case 256: return Layout<256, false, false>::STAGES;
+        default: return 0;
+    }
+}
+
+int gemm_c_box_cols(int bn) {
+    switch (bn) {
+        case 128: return Layout<128, false, false>::EPI_BOX_COLS;
+        case 224: return Layout<224, false, false>::EPI_BOX_COLS;
+        case 256: return Layout<256, false, false>::EPI_BOX_COLS;
         default: return 0;
     }
 }
@@ -727,6 +796,7 @@ int gemm_stages(int bn) {
 int gemm_pair_max_clusters(int bn, bool row_scaled_b) {
     switch (bn) {
         case 128: return row_scaled_b ? pair_max_clusters<128, true>() : pair_max_clusters<128, false>();
+        case 224: return row_scaled_b ? 0 : pair_max_clusters<224, false>();
         case 256: return row_scaled_b ? pair_max_clusters<256, true>() : pair_max_clusters<256, false>();
         default: return 0;
     }
@@ -754,11 +824,13 @@ cudaError_t launch_gemm(const GemmLaunch& g) {
     } else if (g.pair) {
         switch (g.bn) {
             case 128: return launch_one<128, false, true>(g);
+            case 224: return launch_one<224, false, true>(g);
             case 256: return launch_one<256, false, true>(g);
         }
     } else {
         switch (g.bn) {
             case 128: return launch_one<128, false, false>(g);
+            case 224: return launch_one<224, false, false>(g);
             case 256: return launch_one<256, false, false>(g);
         }
     }

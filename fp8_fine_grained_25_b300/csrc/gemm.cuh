@@ -30,7 +30,7 @@ struct GemmLaunch {
     const CUtensorMap* tmB;
     const CUtensorMap* tmC;
     GemmArgs args;
-    int bn;
+    int bn;                  // 128, 224 (dense, block-scaled B) or 256
     bool grouped;
     bool pair;               // 2-CTA clusters with the 2-CTA MMA (dense only)
     bool row_scaled_b;       // sb holds one scale per row of B (dense only)
@@ -40,6 +40,9 @@ struct GemmLaunch {
 
 cudaError_t launch_gemm(const GemmLaunch& g);
 int gemm_stages(int bn);
+// Columns of the TMA-store box of C the kernel writes through (the tensor
+// map's box width; 32 with a 64-byte swizzle, or 16 with a 32-byte swizzle).
+int gemm_c_box_cols(int bn);
 // Pair mode: how many 2-CTA clusters of the dense kernel fit on the device
 // at once (0 if none or on error).
 int gemm_pair_max_clusters(int bn, bool row_scaled_b);

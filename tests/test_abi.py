@@ -203,3 +203,13 @@ def test_ue8m0_quantizer_argument_checks(lib):
         assert f(P, 4, 120, P, P, None) == ALIGN
         assert f(P, 4, 128, P + 8, P, None) == ALIGN
         assert f(P, 4, 128, P, P + 1, None) != ALIGN  # byte scales need no alignment
+
+
+def test_tile_width_setter(lib):
+    # the setters only record a process-wide choice; no device is touched
+    OK, UNSUPPORTED = 0, 7
+    for bn in (0, 128, 224, 256):
+        assert lib.fp8q_set_gemm_tile_n(bn) == OK, bn
+    for bn in (64, 192, 512, -1):
+        assert lib.fp8q_set_gemm_tile_n(bn) == UNSUPPORTED, bn
+    assert lib.fp8q_set_gemm_tile_n(0) == OK

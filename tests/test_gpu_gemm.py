@@ -1,7 +1,7 @@
 """GPU block-scaled GEMM vs the CPU oracle, within
 |C - C_oracle| <= 1 bf16 ulp + 1e-5 * sum_k |a_k b_k|, on ragged small
-shapes (full output), random codes with wide dynamic range, both tile
-widths, and sampled outputs of the full-size workloads."""
+shapes (full output), random codes with wide dynamic range, every tile
+width (128, 224, 256), and sampled outputs of the full-size workloads."""
 import numpy as np
 import pytest
 import torch
@@ -20,6 +20,7 @@ def q():
     mod.fp8q_get_device_status()
     yield mod
     mod.fp8q_set_gemm_tile_n(0)
+    mod.fp8q_set_gemm_pairs(True)
 
 
 def _random_operands(M, N, K, seed):
@@ -51,7 +52,7 @@ SHAPES = [(128, 256, 512), (1, 8, 16), (300, 520, 400), (129, 264, 144), (257, 5
           (640, 1536, 1024), (1000, 2056, 256), (384, 384, 2048)]
 
 
-@pytest.mark.parametrize("bn", [0, 128, 256])
+@pytest.mark.parametrize("bn", [0, 128, 224, 256])
 @pytest.mark.parametrize("M,N,K", SHAPES)
 def test_gemm_random_codes_full_output(q, M, N, K, bn):
     q.fp8q_set_gemm_tile_n(bn)
@@ -63,15 +64,23 @@ def test_gemm_random_codes_full_output(q, M, N, K, bn):
     q.fp8q_set_gemm_tile_n(0)
 
 
-def test_gemm_tile_widths_agree_bitwise(q):
-    # Both tile widths run the same arithmetic per output element.
+@pytest.mark.parametrize("pairs", [True, False])
+def test_gemm_tile_widths_agree_bitwise(q, pairs):
+    # Every tile width runs the same arithmetic per output element. N = 776
+    # puts 224-wide tiles at column offsets 0, 96 and 64 of a 128-column
+    # scale block, and ends in a partial tile.
     qa, sa, qb, sb = _random_operands(333, 776, 1024, 5)
-    q.fp8q_set_gemm_tile_n(128)
-    c1 = _run(q, qa, sa, qb, sb).clone()
-    q.fp8q_set_gemm_tile_n(256)
-    c2 = _run(q, qa, sa, qb, sb)
-    q.fp8q_set_gemm_tile_n(0)
-    assert torch.equal(c1.view(torch.int16), c2.view(torch.int16))
+    q.fp8q_set_gemm_pairs(pairs)
+    try:
+        out = {}
+        for bn in (128, 224, 256):
+            q.fp8q_set_gemm_tile_n(bn)
+            out[bn] = _run(q, qa, sa, qb, sb).clone()
+    finally:
+        q.fp8q_set_gemm_tile_n(0)
+        q.fp8q_set_gemm_pairs(True)
+    assert torch.equal(out[128].view(torch.int16), out[256].view(torch.int16))
+    assert torch.equal(out[224].view(torch.int16), out[256].view(torch.int16))
 
 
 def test_gemm_repeatable(q):
