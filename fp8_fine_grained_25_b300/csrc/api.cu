@@ -99,16 +99,17 @@ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // Output-tile width by a wave model: waves of tiles over the SMs times the
 // tile's cost, its width plus a fixed share for the per-K-block handshake
 // that does not shrink with the width. The shares reproduce measured
-// per-column costs relative to 256: 1.2 for 128 and 1.05 for 224. 224
-// (block-scaled B only) fills whole waves more often at 7168-wide outputs
-// and wastes fewer columns at N = 576; ties keep the earlier candidate.
+// per-column costs relative to 256: 1.2 for 128 and ~1.08 for 224 (in long
+// power-capped runs). 224 (block-scaled B only) wins where it saves a wave
+// or wasted columns (2048 x 7168, N = 576); at 8192 x 7168 its 6 % wave
+// saving does not pay, and 256 stays. Ties keep the earlier candidate.
 int choose_bn(int64_t M, int64_t N, int sms, bool allow224) {
     int best = 256;
     int64_t best_cost = -1;
     for (int bn : {256, 128, 224}) {
         if (bn == 224 && !allow224) continue;
         const int64_t tiles = cdiv(M, 128) * cdiv(N, bn);
-        const int64_t cost = cdiv(tiles, sms) * (bn + (bn == 224 ? 70 : 64));
+        const int64_t cost = cdiv(tiles, sms) * (bn + (bn == 224 ? 80 : 64));
         if (best_cost < 0 || cost < best_cost) {
             best = bn;
             best_cost = cost;
