@@ -88,6 +88,7 @@ struct Layout {
     static constexpr int SCALE_SLOT_BYTES = 4 * kScaleKb * (BM + SB_PER_KB);
     static constexpr int SCALE_BYTES = kScaleSlots * SCALE_SLOT_BYTES;
     static constexpr int NBUF = (512 / BN) > 4 ? 4 : (512 / BN);  // TMEM buffers of BN columns
+    static_assert(NBUF * BN <= 512 && (BN % 32) == 0, "TMEM buffers start on multiples of 32 columns");
     static constexpr int TMEM_COLS = NBUF * BN <= 128 ? 128 : NBUF * BN <= 256 ? 256 : 512;
     static constexpr int RESERVE = 1024 /*alignment slack*/ + 512 /*barriers, flags*/ +
                                    (GROUPED ? 4 * (kMaxExperts + 1) : 0);
@@ -107,8 +108,8 @@ struct Layout {
     static constexpr int HALF = BN / 2;       // columns per promotion warp
     static constexpr int CHUNKS = HALF / 32;  // 32-column TMEM loads, issued in pairs
     static_assert(BN == 128 || BN == 224 || BN == 256, "tile width must be 128, 224 or 256");
-    static_assert(BN != 224 || (!GROUPED && !ROWB), "224-wide tiles are for the block-scaled dense GEMM");
-    static_assert(BN == 224 || CHUNKS % 2 == 0, "32-column TMEM chunks are loaded in pairs");
+    static_assert(HALF % 32 == 0 || (!GROUPED && !ROWB), "224-wide tiles are for the block-scaled dense GEMM");
+    static_assert(HALF % 32 == 16 || CHUNKS % 2 == 0, "32-column TMEM chunks are loaded in pairs");
     static_assert((B_ROWS * BK) % 1024 == 0 && STAGE_BYTES % 1024 == 0,
                   "stages and their B tiles must start on 1024-byte swizzle atoms");
     static_assert(!(PAIR && GROUPED), "pair mode is for the dense GEMM");
@@ -217,22 +218,25 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 }
 
 // acc[O .. O + NCOL) += P * c, packed.
-template <int O, int NCOL>
-__device__ __forceinline__ void fma_cols(float (&acc)[112], const uint32_t* r, float c) {
+template <int O, int NCOL, int HALF>
+__device__ __forceinline__ void fma_cols(float (&acc)[HALF], const uint32_t* r, float c) {
 #pragma unroll
     for (int i = 0; i < NCOL; i += 2) ffma2(acc[O + i], acc[O + i + 1], r[i], r[i + 1], c);
 }
 
-// Promotion of one warp's 112 columns of a 224-wide tile, the same code for
-// both warpgroups (h): 32-column chunks at warp columns b, b + 32, b + 64
-// (b = 16 h) into acc[0, 96), and a 16-column chunk at column 96 - 96 h into
-// acc[96, 112). Every 32-column chunk then starts on a multiple of 32 (the
-// tile starts on one; a warpgroup's 112 columns leave 16 over), so none
-// crosses a 128-column scale block: a chunk at warp column o uses cs when
-// o < split, else csn. Two TMEM loads per wait.
-__device__ __forceinline__ void promote_112(float (&acc)[112], uint32_t taddr, int h, float cs,
+// Promotion of one warp's HALF columns when HALF = 16 mod 32 (112 of a
+// 224-wide tile), the same code for both warpgroups (h):
+// 32-column chunks at warp columns b + 32 i (b = 16 h) into acc[32 i, +32),
+// i < HALF / 32, and a 16-column chunk at column (HALF - 16) (1 - h) into
+// acc[HALF - 16, HALF). Every 32-column chunk then starts on a multiple of 32
+// (the tile starts on one; a warpgroup's HALF columns leave 16 over), so
+// none crosses a 128-column scale block: a chunk at warp column o uses cs
+// when o < split, else csn. Two TMEM loads per wait.
+template <int HALF>
+__device__ __forceinline__ void promote_odd(float (&acc)[HALF], uint32_t taddr, int h, float cs,
                                             float csn, int split) {
-    const int b = 16 * h, o16 = 96 - 96 * h;
+    static_assert(HALF == 112, "112 columns per warp");
+    const int b = 16 * h, o16 = (HALF - 16) * (1 - h);
     uint32_t r0[32], r1[32];
     tmem_ld32(taddr + b, r0);
     tmem_ld32(taddr + b + 32, r1);
@@ -244,7 +248,7 @@ __device__ __forceinline__ void promote_112(float (&acc)[112], uint32_t taddr, i
     tmem_ld16(taddr + o16, r3);
     tmem_wait_ld48(r2, r3);
     fma_cols<64, 32>(acc, r2, b + 64 < split ? cs : csn);
-    fma_cols<96, 16>(acc, r3, o16 < split ? cs : csn);
+    fma_cols<HALF - 16, 16>(acc, r3, o16 < split ? cs : csn);
 }
 
 template <int BN, bool GROUPED, bool PAIR, bool ROWB>
@@ -517,6 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t abuf = 0, aphase = 0;
         int slot = 0;
         uint32_t sphase = 0;
+        uint32_t ebox = 0;  // epilogue boxes staged so far: their buffer alternates
         bool ok = true;
         const uint32_t temptry_base = PAIR ? mapa_shared(bar(L::TEMPTY), 0) : bar(L::TEMPTY);
         for (int t = unit0; ok && t < num_tiles; t += unit_step) {
@@ -554,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         sb_cols = sl + kScaleKb * BM + h * L::HALF;
                     } else {
                         sb4 = *reinterpret_cast<const float4*>(sl + 4 * (BM + rel_nb));
-                        if constexpr (BN == 224)
+                        if constexpr (L::HALF % 32 == 16)
                             sb4n = *reinterpret_cast<const float4*>(sl + 4 * (BM + rel_nb + 1));
                         __syncwarp();
                         if (lane == 0) mbar_arrive(bar(L::SEMPTY + slot));
@@ -568,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float b_s = j == 0 ? sb4.x : j == 1 ? sb4.y : j == 2 ? sb4.z : sb4.w;
                 const float cs = a_s * b_s;
                 const float b_sn = j == 0 ? sb4n.x : j == 1 ? sb4n.y : j == 2 ? sb4n.z : sb4n.w;
-                const float csn = a_s * b_sn;  // BN = 224: the warp's second block
+                const float csn = a_s * b_sn;  // 224-wide tiles: the warp's second block
 
                 if (!warp_wait<PAIR>(bar(L::TFULL + abuf), aphase, abort_flag, limit)) {
                     ok = false;
@@ -596,8 +601,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ffma2_cols(a[2], a[3], r0[4 * i + 2], r0[4 * i + 3], a_s, b[i].z, b[i].w);
                         }
                     }
-                } else if constexpr (BN == 224) {
-                    promote_112(acc, taddr, h, cs, csn, split);
+                } else if constexpr (L::HALF % 32 == 16) {
+                    promote_odd<L::HALF>(acc, taddr, h, cs, csn, split);
                 } else {
 #pragma unroll
                     for (int c = 0; c < L::CHUNKS; c += 2) {
@@ -641,17 +646,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // box holds EPI_BOX_COLS / 8 16-byte pieces; piece j sits at
                 // j ^ (r / 2 % 4) for the 64-byte swizzle (32 columns) and at
                 // j ^ (r / 4 % 2) for the 32-byte swizzle (16 columns). Box c2
-                // stores acc[BC c2, +BC); for BN = 224 those are warp columns
-                // 16 h + 16 c2 for c2 < 6 and 96 - 96 h for c2 = 6 (the
-                // promotion's chunk order).
+                // stores acc[BC c2, +BC); when HALF = 16 mod 32 those are warp
+                // columns 16 h + 16 c2, and HALF - 16 - (HALF - 16) h for the
+                // last box (the promotion's chunk order).
                 constexpr int BC = L::EPI_BOX_COLS;
                 uint8_t* ebuf0 = smem + L::EPI_OFF + ew * L::EPI_WARP_BYTES;
                 const uint32_t ebuf0_s = sbase + L::EPI_OFF + ew * L::EPI_WARP_BYTES;
 #pragma unroll
                 for (int c2 = 0; c2 < L::HALF / BC; ++c2) {
-                    uint8_t* ebuf = ebuf0 + (c2 & 1) * L::EPI_BOX_BYTES;
-                    const uint32_t ebuf_s = ebuf0_s + (c2 & 1) * L::EPI_BOX_BYTES;
-                    // the store issued two boxes ago (same buffer) must have read it
+                    const uint32_t eb = ebox++ & 1u;  // across tiles too (odd box counts)
+                    uint8_t* ebuf = ebuf0 + eb * L::EPI_BOX_BYTES;
+                    const uint32_t ebuf_s = ebuf0_s + eb * L::EPI_BOX_BYTES;
+                    // the store issued two boxes ago (same buffer) must have read
+                    // it: every box commits one bulk group, so at most the previous
+                    // box's may still be reading
                     if (lane == 0) bulk_wait_group_read1();
                     __syncwarp();
 #pragma unroll
@@ -667,11 +675,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
-                    const int wc = BN != 224 ? BC * c2 : c2 < 6 ? 16 * h + 16 * c2 : 96 - 96 * h;
+                    const int wc = L::HALF % 32 == 0 ? BC * c2
+                                   : c2 < L::HALF / 16 - 1 ? 16 * h + 16 * c2
+                                                          : (L::HALF - 16) * (1 - h);
                     const int x = col0 + wc, y = tile.m0 + quarter * 32;
-                    if (lane == 0 && x < args.N && y < args.M) {
-                        tma_store_2d(&tmC, ebuf_s, x, y);
-                        bulk_commit_group();
+                    if (lane == 0) {
+                        if (x < args.N && y < args.M) tma_store_2d(&tmC, ebuf_s, x, y);
+                        bulk_commit_group();  // empty when the box lies past C
                     }
                 }
             } else {

@@ -375,6 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t ebuf0_s = sbase + L::EPI_OFF + ew * L::EPI_WARP_BYTES;
         const uint32_t tempty_base = lead_bar(L::TEMPTY);
         uint32_t abuf = 0, aphase = 0;
+        uint32_t ebox = 0;  // boxes staged so far: their buffer alternates, across tiles too
         for (int u = unit0; u < args.num_units; u += unit_step) {
             int m0, n0;
             tile_of<PAIR>(args, u, rank, m0, n0);
@@ -393,9 +394,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         else mbar_arrive(bar(L::TEMPTY + abuf));
                     }
                 }
-                uint8_t* ebuf = ebuf0 + (c & 1) * L::EPI_BOX_BYTES;
-                const uint32_t ebuf_s = ebuf0_s + (c & 1) * L::EPI_BOX_BYTES;
-                // the store issued two boxes ago (same buffer) must have read it
+                const uint32_t eb = ebox++ & 1u;
+                uint8_t* ebuf = ebuf0 + eb * L::EPI_BOX_BYTES;
+                const uint32_t ebuf_s = ebuf0_s + eb * L::EPI_BOX_BYTES;
+                // the store issued two boxes ago (same buffer) must have read it:
+                // every box commits one bulk group, so at most the previous box's
+                // may still be reading
                 if (lane == 0) bulk_wait_group_read1();
                 __syncwarp();
 #pragma unroll
@@ -411,9 +415,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fence_proxy_async_smem();
                 __syncwarp();
                 const int x = n0 + 32 * c, y = m0 + 32 * static_cast<int>(quarter);
-                if (lane == 0 && x < args.N && y < args.M) {
-                    tma_store_2d(&tmC, ebuf_s, x, y);
-                    bulk_commit_group();
+                if (lane == 0) {
+                    if (x < args.N && y < args.M) tma_store_2d(&tmC, ebuf_s, x, y);
+                    bulk_commit_group();  // empty when the box lies past C
                 }
             }
             abuf ^= 1u;

@@ -210,6 +210,6 @@ def test_tile_width_setter(lib):
     OK, UNSUPPORTED = 0, 7
     for bn in (0, 128, 224, 256):
         assert lib.fp8q_set_gemm_tile_n(bn) == OK, bn
-    for bn in (64, 192, 512, -1):
+    for bn in (64, 160, 192, 512, -1):
         assert lib.fp8q_set_gemm_tile_n(bn) == UNSUPPORTED, bn
     assert lib.fp8q_set_gemm_tile_n(0) == OK
