@@ -28,6 +28,13 @@
 // of earlier ones. Every wait is bounded in time; on expiry the CTA raises
 // an abort flag, drains its copies and MMAs, frees TMEM and returns.
 //
+// Tile width 224 (block-scaled dense GEMM only) fills whole waves of 7168-
+// wide outputs and wastes fewer columns at N = 576. Such a tile starts on a
+// multiple of 32 but not of 128: the scale ring carries up to three
+// 128-column B-scale blocks, each promotion warp's 112 columns touch at most
+// two (two scale products per K block), and the warp reads TMEM in 32-column
+// chunks that start on multiples of 32 plus one 16-column chunk.
+//
 // Pair mode (dense GEMM): two CTAs of a cluster compute a 256 x BN tile with
 // the 2-CTA MMA (tcgen05 cta_group::2). Each CTA holds its own 128 rows of A
 // and half of the tile's B rows, so each SM's shared memory carries 32 KB
