@@ -446,18 +446,21 @@ def time_alone(path, names, device, reps: int = 25):
 
 
 # --------------------------------------------------------------- CPU oracle
-def oracle_sample(w, rows_a: int, out_rows: int, threads: int):
+def oracle_sample(w, rows_a: int, w_rows: int, out_rows: int, threads: int):
     """Time the CPU oracle on a bounded sample of one step and extrapolate
-    the full step: quantizer time scales with elements, GEMM time with
-    output elements. Returns (seconds for a full step, description)."""
+    the full step: quant_act on `rows_a` rows of A, quant_weight on the first
+    `w_rows` rows of the (first) weight, and the GEMM of `out_rows` rows of A
+    against those weight rows; each part scaled by its element count.
+    Returns (seconds for a full step, description)."""
     import numpy as np
     import oracle
     A = w.A
     M, K = A.shape
     Wd = w.weights["W"][0] if w.offsets is not None else next(iter(w.weights.values()))
     N = Wd.shape[0]
+    w_rows, out_rows = min(w_rows, N), min(out_rows, rows_a)
     bits = lambda t: t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
-    a_s = bits(A[:rows_a])
+    a_s, b_s = bits(A[:rows_a]), bits(Wd[:w_rows])
     pow2 = w.scales == "ue8m0"
     qact = oracle.quant_act_ue8m0 if pow2 else oracle.quant_act
     qweight = oracle.quant_weight_ue8m0 if pow2 else oracle.quant_weight
@@ -465,32 +468,35 @@ def oracle_sample(w, rows_a: int, out_rows: int, threads: int):
     t0 = time.perf_counter()
     qa, sa = qact(a_s, threads=threads)
     t1 = time.perf_counter()
-    qb_full, sb_full = qweight(bits(Wd), threads=threads)  # GEMM needs all of B
+    qb, sb = qweight(b_s, threads=threads)
     t2 = time.perf_counter()
-    c32, S = gemm(qa, sa, qb_full, sb_full, rows=np.arange(min(out_rows, rows_a)), threads=threads)
+    gemm(qa, sa, qb, sb, rows=np.arange(out_rows), threads=threads)
     t3 = time.perf_counter()
     w_elems = sum(W.numel() for W in w.weights.values())
     full = ((t1 - t0) * (M * K) / a_s.size
-            + (t2 - t1) * w_elems / Wd.numel()
-            + (t3 - t2) * (step_flops(w) / (2.0 * min(out_rows, rows_a) * N * K)))
-    desc = (f"oracle quant_act on {rows_a}x{K} rows, quant_weight on one [{N}x{K}] weight, "
-            f"GEMM on {min(out_rows, rows_a)} output rows x {N} columns; "
-            f"sample took {t3 - t0:.2f} s, full step extrapolated by element counts")
+            + (t2 - t1) * w_elems / b_s.size
+            + (t3 - t2) * (step_flops(w) / (2.0 * out_rows * w_rows * K)))
+    desc = (f"oracle quant_act on {rows_a}x{K}, quant_weight on {w_rows}x{K} of a [{N}x{K}] weight, "
+            f"GEMM on {out_rows} x {w_rows} outputs; sample took {t3 - t0:.2f} s, full step "
+            "extrapolated by element counts")
     return full, desc
 
 
-def oracle_sample_backward(w, rows: int, cols: int, out_rows: int, threads: int):
+def oracle_sample_backward(w, rows: int, cols: int, out_rows: int, w_cols: int, threads: int):
     """The same for the backward step: quant_act on `rows` rows of dY, the
-    transposed weight quantization on all of W, the dX GEMM on `out_rows`
-    output rows, quant_act_t on `cols` columns of dY and of X, and the dW
-    GEMM on out_rows x cols outputs; each part scaled by its element count."""
+    transposed weight quantization on the first `w_cols` columns of W, the
+    dX GEMM on out_rows x w_cols outputs, quant_act_t on `cols` columns of dY
+    and of X, and the dW GEMM on out_rows x cols outputs; each part scaled by
+    its element count."""
     import numpy as np
     import oracle
     dY, X, W = w.A, w.X, w.weights["W"]
     T, N = dY.shape
     K = X.shape[1]
+    w_cols = min(w_cols, K)
     bits = lambda t: t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
-    dy_rows, dy_cols, x_cols, w_bits = bits(dY[:rows]), bits(dY[:, :cols]), bits(X[:, :cols]), bits(W)
+    dy_rows, dy_cols, x_cols = bits(dY[:rows]), bits(dY[:, :cols]), bits(X[:, :cols])
+    w_part = bits(W[:, :w_cols])
     u = w.scales == "ue8m0"
     qact = oracle.quant_act_ue8m0 if u else oracle.quant_act
     qwt = oracle.quant_weight_t_ue8m0 if u else oracle.quant_weight_t
@@ -500,7 +506,7 @@ def oracle_sample_backward(w, rows: int, cols: int, out_rows: int, threads: int)
     t = [time.perf_counter()]
     qdy, sdy = qact(dy_rows, threads=threads)
     t.append(time.perf_counter())
-    _, _, qwt_, swt_ = qwt(w_bits, threads=threads)
+    _, _, qwt_, swt_ = qwt(w_part, threads=threads)
     t.append(time.perf_counter())
     gemm(qdy, sdy, qwt_, swt_, rows=np.arange(out_rows), threads=threads)
     t.append(time.perf_counter())
@@ -511,26 +517,35 @@ def oracle_sample_backward(w, rows: int, cols: int, out_rows: int, threads: int)
     wgrad(qdyt, sdyt, qxt, sxt, rows=np.arange(out_rows), threads=threads)
     t.append(time.perf_counter())
     d = np.diff(t)
-    full = (d[0] * T / rows + d[1] + d[2] * T / out_rows + d[3] * N / cols + d[4] * K / cols
-            + d[5] * (N * K) / (out_rows * cols))
-    desc = (f"oracle quant_act on {rows} rows of dY, quant_weight_t on all of W, dX GEMM on "
-            f"{out_rows} rows x {K} columns, quant_act_t on {cols} columns of dY and of X, dW GEMM "
-            f"on {out_rows} x {cols} outputs; sample took {t[-1] - t[0]:.2f} s, full step "
+    full = (d[0] * T / rows + d[1] * K / w_cols + d[2] * (T * K) / (out_rows * w_cols)
+            + d[3] * N / cols + d[4] * K / cols + d[5] * (N * K) / (out_rows * cols))
+    desc = (f"oracle quant_act on {rows} rows of dY, quant_weight_t on {w_cols} columns of W, dX "
+            f"GEMM on {out_rows} x {w_cols} outputs, quant_act_t on {cols} columns of dY and of X, "
+            f"dW GEMM on {out_rows} x {cols} outputs; sample took {t[-1] - t[0]:.2f} s, full step "
             "extrapolated by element counts")
     return full, desc
 
 
-def sample_oracle(w, small: bool, threads: int):
-    """The bounded oracle sample of one step of workload w (small: the
-    reference arm's per-step sample)."""
+# Oracle sample sizes, largest first: (rows of A, weight rows, GEMM rows) for
+# a forward step, (rows of dY, columns of dY/X, GEMM rows, columns of W) for a
+# backward one. Tier 0 is the cpu_baseline sample (about 10-30 s of oracle
+# work on an 8- to 16-core host); the reference arm takes the largest tier
+# that lets all of its steps finish within its time budget. Smaller samples
+# extrapolate to a slower oracle (fixed costs scale up with them).
+SAMPLE_TIERS = [(4096, 1 << 30, 3072), (2048, 1024, 256), (1024, 512, 128), (512, 256, 64),
+                (64, 128, 8)]
+SAMPLE_TIERS_BACKWARD = [(4096, 2048, 1536, 1 << 30), (2048, 1024, 256, 1024), (1024, 512, 128, 512),
+                         (512, 256, 64, 256), (64, 128, 8, 128)]
+
+
+def sample_oracle(w, tier: int, threads: int):
+    """The bounded oracle sample of one step of workload w at a size tier."""
     if w.X is not None:
-        if small:
-            return oracle_sample_backward(w, rows=64, cols=128, out_rows=4, threads=threads)
-        return oracle_sample_backward(w, rows=4096, cols=2048, out_rows=1536, threads=threads)
-    if small:
-        return oracle_sample(w, rows_a=64, out_rows=4, threads=threads)
-    # about 10-30 s of oracle work on an 8- to 16-core host
-    return oracle_sample(w, rows_a=4096, out_rows=3072, threads=threads)
+        rows, cols, out_rows, w_cols = SAMPLE_TIERS_BACKWARD[tier]
+        return oracle_sample_backward(w, rows=rows, cols=cols, out_rows=out_rows, w_cols=w_cols,
+                                      threads=threads)
+    rows_a, w_rows, out_rows = SAMPLE_TIERS[tier]
+    return oracle_sample(w, rows_a=rows_a, w_rows=w_rows, out_rows=out_rows, threads=threads)
 
 
 def run_reference(args, rank, world):
@@ -540,10 +555,20 @@ def run_reference(args, rank, world):
     threads = os.cpu_count() or 1
     w = make_workload(args.config, "cpu")
     flops = step_flops(w)
+    # the largest sample tier whose first step, repeated for the whole run,
+    # fits the budget (tier 0 is the cpu_baseline sample, too large here)
+    budget_s = 150.0
+    tier = 1
+    while True:
+        t0 = time.perf_counter()
+        sample_oracle(w, tier, threads)
+        if (time.perf_counter() - t0) * (args.warmup + args.steps) <= budget_s or tier == len(SAMPLE_TIERS) - 1:
+            break
+        tier += 1
     times = []
     desc = ""
     for i in range(args.warmup + args.steps):
-        full, desc = sample_oracle(w, small=True, threads=threads)
+        full, desc = sample_oracle(w, tier, threads)
         if i >= args.warmup:
             times.append(full)
     t = statistics.median(times)
@@ -736,7 +761,7 @@ def main():
     cpu = None
     if rank == 0 and world == 1:
         threads = os.cpu_count() or 1
-        full, desc = sample_oracle(w, small=False, threads=threads)
+        full, desc = sample_oracle(w, 0, threads)
         cpu = {"value": flops / full / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                "sample": desc}
 
