@@ -446,11 +446,19 @@ def time_alone(path, names, device, reps: int = 25):
 
 
 # --------------------------------------------------------------- CPU oracle
+def _busy(units: int, threads: int) -> float:
+    """Fraction of the oracle's host threads a call over `units` independent
+    rows (or row blocks) keeps busy: the oracle splits them over threads."""
+    return min(units, threads) / threads
+
+
 def oracle_sample(w, rows_a: int, w_rows: int, out_rows: int, threads: int):
     """Time the CPU oracle on a bounded sample of one step and extrapolate
     the full step: quant_act on `rows_a` rows of A, quant_weight on the first
     `w_rows` rows of the (first) weight, and the GEMM of `out_rows` rows of A
-    against those weight rows; each part scaled by its element count.
+    against those weight rows. Each part scales by its work ratio and by the
+    share of threads the sample kept busy (a sample with fewer rows than
+    threads runs on fewer threads than the full step would).
     Returns (seconds for a full step, description)."""
     import numpy as np
     import oracle
@@ -473,12 +481,12 @@ def oracle_sample(w, rows_a: int, w_rows: int, out_rows: int, threads: int):
     gemm(qa, sa, qb, sb, rows=np.arange(out_rows), threads=threads)
     t3 = time.perf_counter()
     w_elems = sum(W.numel() for W in w.weights.values())
-    full = ((t1 - t0) * (M * K) / a_s.size
-            + (t2 - t1) * w_elems / b_s.size
-            + (t3 - t2) * (step_flops(w) / (2.0 * out_rows * w_rows * K)))
+    full = ((t1 - t0) * (M * K) / a_s.size * _busy(rows_a, threads)
+            + (t2 - t1) * w_elems / b_s.size * _busy(-(-w_rows // 128), threads)
+            + (t3 - t2) * (step_flops(w) / (2.0 * out_rows * w_rows * K)) * _busy(out_rows, threads))
     desc = (f"oracle quant_act on {rows_a}x{K}, quant_weight on {w_rows}x{K} of a [{N}x{K}] weight, "
             f"GEMM on {out_rows} x {w_rows} outputs; sample took {t3 - t0:.2f} s, full step "
-            "extrapolated by element counts")
+            "extrapolated by work, per busy thread")
     return full, desc
 
 
@@ -486,8 +494,8 @@ def oracle_sample_backward(w, rows: int, cols: int, out_rows: int, w_cols: int, 
     """The same for the backward step: quant_act on `rows` rows of dY, the
     transposed weight quantization on the first `w_cols` columns of W, the
     dX GEMM on out_rows x w_cols outputs, quant_act_t on `cols` columns of dY
-    and of X, and the dW GEMM on out_rows x cols outputs; each part scaled by
-    its element count."""
+    and of X, and the dW GEMM on out_rows x cols outputs; each part scaled as
+    in oracle_sample."""
     import numpy as np
     import oracle
     dY, X, W = w.A, w.X, w.weights["W"]
@@ -517,12 +525,14 @@ def oracle_sample_backward(w, rows: int, cols: int, out_rows: int, w_cols: int, 
     wgrad(qdyt, sdyt, qxt, sxt, rows=np.arange(out_rows), threads=threads)
     t.append(time.perf_counter())
     d = np.diff(t)
-    full = (d[0] * T / rows + d[1] * K / w_cols + d[2] * (T * K) / (out_rows * w_cols)
-            + d[3] * N / cols + d[4] * K / cols + d[5] * (N * K) / (out_rows * cols))
+    b = lambda units: _busy(units, threads)
+    full = (d[0] * T / rows * b(rows) + d[1] * K / w_cols + d[2] * (T * K) / (out_rows * w_cols) * b(out_rows)
+            + d[3] * N / cols * b(cols) + d[4] * K / cols * b(cols)
+            + d[5] * (N * K) / (out_rows * cols) * b(out_rows))
     desc = (f"oracle quant_act on {rows} rows of dY, quant_weight_t on {w_cols} columns of W, dX "
             f"GEMM on {out_rows} x {w_cols} outputs, quant_act_t on {cols} columns of dY and of X, "
             f"dW GEMM on {out_rows} x {cols} outputs; sample took {t[-1] - t[0]:.2f} s, full step "
-            "extrapolated by element counts")
+            "extrapolated by work, per busy thread")
     return full, desc
 
 
@@ -531,7 +541,7 @@ def oracle_sample_backward(w, rows: int, cols: int, out_rows: int, w_cols: int, 
 # backward one. Tier 0 is the cpu_baseline sample (about 10-30 s of oracle
 # work on an 8- to 16-core host); the reference arm takes the largest tier
 # that lets all of its steps finish within its time budget. Smaller samples
-# extrapolate to a slower oracle (fixed costs scale up with them).
+# still extrapolate to a somewhat slower oracle (per-call costs scale up).
 SAMPLE_TIERS = [(4096, 1 << 30, 3072), (2048, 1024, 256), (1024, 512, 128), (512, 256, 64),
                 (64, 128, 8)]
 SAMPLE_TIERS_BACKWARD = [(4096, 2048, 1536, 1 << 30), (2048, 1024, 256, 1024), (1024, 512, 128, 512),
@@ -557,7 +567,7 @@ def run_reference(args, rank, world):
     flops = step_flops(w)
     # the largest sample tier whose first step, repeated for the whole run,
     # fits the budget (tier 0 is the cpu_baseline sample, too large here)
-    budget_s = 150.0
+    budget_s = 240.0
     tier = 1
     while True:
         t0 = time.perf_counter()
