@@ -22,6 +22,7 @@ def q():
     mod.fp8q_set_fault_injection(0)
     mod.fp8q_set_wait_timeout_ns(0)
     mod.fp8q_set_gemm_pairs(True)
+    mod.fp8q_set_gemm_tile_n(0)
 
 
 def _ops(M, N, K, seed):
@@ -34,9 +35,11 @@ def _ops(M, N, K, seed):
     return (qa, sa, qb, sb), (t(qa), t(sa), t(qb), t(sb))
 
 
+@pytest.mark.parametrize("bn", [0, 224])
 @pytest.mark.parametrize("pairs", [True, False])
-def test_stalled_stage_times_out_and_context_survives(q, pairs):
+def test_stalled_stage_times_out_and_context_survives(q, pairs, bn):
     q.fp8q_set_gemm_pairs(pairs)
+    q.fp8q_set_gemm_tile_n(bn)
     host, dev = _ops(512, 512, 1024, 1)
     q.fp8q_set_wait_timeout_ns(20_000_000)  # 20 ms per wait
     q.fp8q_set_fault_injection(q.INJECT_STALLED_STAGE)
