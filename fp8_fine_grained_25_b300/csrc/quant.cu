@@ -694,10 +694,13 @@ __device__ __forceinline__ void load_weight_block(const WeightPlainArgs& a, uint
 
 template <bool WQ, bool WT, bool POW2>  // POW2: UE8M0 scales
 __global__ void __launch_bounds__(kTThreads, 2) quant_weight_plain_kernel(const WeightPlainArgs a) {
-    __shared__ uint32_t red[8];
-    __shared__ float2 sr_sh;  // the block's scale and reciprocal (0: IEEE-divide range)
+    // per-warp partial maxima, double-buffered by block parity: one barrier
+    // per block, after which every thread forms the block scale itself (a
+    // warp can be at most one block ahead of the slowest one)
+    __shared__ uint32_t red[2][8];
     const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
     const uint32_t nblocks = a.NB * a.KB;
+    uint32_t par = 0;
     uint2 v[16];
     if (blockIdx.x < nblocks) load_weight_block<WT>(a, blockIdx.x, w, l, v);
     for (uint32_t b = blockIdx.x; b < nblocks; b += gridDim.x) {
@@ -713,18 +716,19 @@ __global__ void __launch_bounds__(kTThreads, 2) quant_weight_plain_kernel(const 
         mx = max(mx & 0xFFFFu, mx >> 16);
 #pragma unroll
         for (int d = 16; d >= 1; d >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, d));
-        if (l == 0) red[w] = mx;
+        if (l == 0) red[par][w] = mx;
         __syncthreads();
-        if (threadIdx.x == 0) {
-            uint32_t m = red[0];
+        uint32_t m = red[par][0];
 #pragma unroll
-            for (int i = 1; i < 8; ++i) m = max(m, red[i]);
-            const float amax = __uint_as_float(m << 16);
-            float sc, rc;
-            bool fast;
-            uint32_t byte;
-            tile_scale_for<POW2>(amax, sc, rc, fast, byte);
-            sr_sh = make_float2(sc, fast ? rc : 0.0f);
+        for (int i = 1; i < 8; ++i) m = max(m, red[par][i]);
+        par ^= 1u;
+        const float amax = __uint_as_float(m << 16);
+        float sc, rc;
+        bool fast;
+        uint32_t byte;
+        tile_scale_for<POW2>(amax, sc, rc, fast, byte);
+        const float2 sr = make_float2(sc, fast ? rc : 0.0f);
+        if (threadIdx.x == 0) {
             if constexpr (POW2) {
                 if constexpr (WQ) a.s8[static_cast<uint64_t>(nb) * a.KB + kb] = static_cast<uint8_t>(byte);
                 if constexpr (WT) a.st8[static_cast<uint64_t>(kb) * a.NB + nb] = static_cast<uint8_t>(byte);
@@ -733,8 +737,6 @@ __global__ void __launch_bounds__(kTThreads, 2) quant_weight_plain_kernel(const 
                 if constexpr (WT) a.st[static_cast<uint64_t>(kb) * a.NB + nb] = sc;
             }
         }
-        __syncthreads();
-        const float2 sr = sr_sh;
         if (k < a.K && sr.x != 0.0f) {
             const float4 s4 = make_float4(sr.x, sr.x, sr.x, sr.x);
             const float4 r4 = make_float4(sr.y, sr.y, sr.y, sr.y);
