@@ -420,12 +420,13 @@ def make_path(w, device):
 
 
 def time_alone(path, names, device, reps: int = 25):
-    """Mean seconds of each named kernel launched by itself, with a 256 MB
-    read just before it so that the L2 holds no dirty lines (inside the step
-    a quantizer also writes back the previous kernel's output) and none of
-    its input. CUDA event timestamps on the B300 advance in steps of
-    2.048 us, so one launch of ~30 us is timed to +-7 %; the mean over `reps`
-    launches averages that out (a median would stay on the 2.048 us grid)."""
+    """Seconds of each named kernel launched by itself, with a 256 MB read
+    just before it so that the L2 holds no dirty lines (inside the step a
+    quantizer also writes back the previous kernel's output) and none of its
+    input. CUDA event timestamps on the B300 advance in steps of 2.048 us, so
+    one launch of ~30 us is timed to +-7 %: the result is the mean of the
+    middle 15 of `reps` launches, which averages that out (a median would
+    stay on the 2.048 us grid) and drops outliers (a plain mean would not)."""
     clean = torch.ones(256 << 20, dtype=torch.uint8, device=device)
     out = {}
     for n in names:
@@ -440,7 +441,8 @@ def time_alone(path, names, device, reps: int = 25):
             e1.record()
             torch.cuda.synchronize()
             ts.append(e0.elapsed_time(e1) / 1e3)
-        out[n] = statistics.fmean(ts)
+        ts.sort()
+        out[n] = statistics.fmean(ts[(reps - 15) // 2:(reps - 15) // 2 + 15])
     del clean
     return out
 
