@@ -93,9 +93,6 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Output-tile width: the one with the fewest tile-width units of work per
-// SM after rounding up to whole waves (a tile of width BN costs BN + 64
-// units: the fixed part is the 128-row A traffic and the per-tile epilogue).
 // Output-tile width by a wave model: waves of tiles over the SMs times the
 // tile's cost, its width plus a fixed share for the per-K-block handshake
 // that does not shrink with the width. The shares reproduce measured
