@@ -695,8 +695,12 @@ __device__ __forceinline__ void load_weight_block(const WeightPlainArgs& a, uint
 template <bool WQ, bool WT, bool POW2>  // POW2: UE8M0 scales
 __global__ void __launch_bounds__(kTThreads, 2) quant_weight_plain_kernel(const WeightPlainArgs a) {
     // per-warp partial maxima, double-buffered by block parity: one barrier
-    // per block, after which every thread forms the block scale itself (a
-    // warp can be at most one block ahead of the slowest one)
+    // per block, after which every thread forms the block scale itself.
+    // Why one barrier suffices: a warp writes red[p] for block b + 2 only
+    // after it has passed the barrier of block b + 1, and every warp reads
+    // red[p] for block b before it arrives at that barrier, so no write to a
+    // buffer can land while another warp still reads that buffer's previous
+    // contents (a warp is at most one block ahead of the slowest one).
     __shared__ uint32_t red[2][8];
     const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
     const uint32_t nblocks = a.NB * a.KB;
