@@ -280,8 +280,14 @@ def job_throughput(world: int, flops_per_step: float, steps: int, seconds: float
 
 
 # ---------------------------------------------------------------- workloads
-def make_workload(config: int, device):
+def make_workload(config: int, device, experts: int = 0):
+    """The workload of `config`; for the MoE configs (4, 7) `experts` > 0
+    keeps `experts` of the 256 routed experts and the same tokens per expert
+    (T = 4096 * experts / 256), a smaller case of the same layer."""
     from fp8_fine_grained_25_b300 import workloads
+    if experts and config in (4, 7):
+        return workloads.WORKLOADS[config](seed=0, device=device, E=experts,
+                                           T=max(workloads.TOP_K, 4096 * experts // workloads.N_ROUTED))
     return workloads.WORKLOADS[config](seed=0, device=device)
 
 
@@ -330,6 +336,14 @@ class Path:
                 sb = torch.empty((-(-W.shape[0] // 128), -(-K // 128)), dtype=sdt, device=device)
                 C = torch.empty((M, W.shape[0]), dtype=torch.bfloat16, device=device)
             self.bufs[name] = (qb, sb, C)
+        # split-K workspace of each dense FP32-scale GEMM whose shape splits
+        # (the MLA down-projections); none for shapes that do not
+        self.ws = {}
+        if w.offsets is None and not self.ue8m0:
+            for name, W in w.weights.items():
+                n = fp8q.fp8_block_gemm_workspace_size(M, W.shape[0], K)
+                if n > 0:
+                    self.ws[name] = torch.empty(n, dtype=torch.uint8, device=device)
         self.launches_per_step = 1 + 2 * len(w.weights)
         # FP8 dispatch: quantize the T tokens, then gather rows into expert order
         self.dispatch = args_dispatch(w)
@@ -392,6 +406,8 @@ class Path:
                 f.fp8_grouped_gemm(self.qa, self.sa, qb, sb, self.w.offsets, C, stream=stream)
             elif self.ue8m0:
                 f.fp8_block_gemm_ue8m0(self.qa, self.sa, qb, sb, C, stream=stream)
+            elif name in self.ws:
+                f.fp8_block_gemm_ws(self.qa, self.sa, qb, sb, C, workspace=self.ws[name], stream=stream)
             else:
                 f.fp8_block_gemm(self.qa, self.sa, qb, sb, C, stream=stream)
             rec(i)
@@ -691,7 +707,7 @@ def run_reference(args, rank, world):
     if rank != 0:
         return
     threads = os.cpu_count() or 1
-    w = make_workload(args.config, "cpu")
+    w = make_workload(args.config, "cpu", args.experts)
     flops = step_flops(w)
     # the largest sample tier whose first step, repeated for the whole run,
     # fits the budget (tier 0 is the cpu_baseline sample, too large here)
@@ -829,6 +845,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5, 6, 7, 8, 9, 10])
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--experts", type=int, default=0,
+                    help="MoE configs: keep this many experts (same tokens per expert)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -850,7 +868,7 @@ def main():
     torch.cuda.set_device(device)
     peaks, peak_kind = load_peaks()
 
-    w = make_workload(args.config, device)
+    w = make_workload(args.config, device, args.experts)
     path = make_path(w, device)
     flops = path.flops
     stream = torch.cuda.current_stream()

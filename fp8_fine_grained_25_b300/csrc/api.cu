@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "fp8q.h"
@@ -34,6 +36,9 @@ DeviceInfo g_devices[kMaxDevices];
 std::mutex g_mutex;
 uint64_t g_timeout_ns = 1000000000ull;
 int g_force_bn = 0;
+int g_force_splits = 0;  // 0: the split-K choice below; else this many K ranges
+constexpr int kMaxSplits = 8;
+std::atomic<uint32_t> g_epoch{0};
 int g_pair_mode = 1;  // 1: use 2-CTA pairs for the dense GEMM where they fit
 uint32_t g_inject = 0;  // FP8Q_INJECT_* bits for failure-path tests
 constexpr int64_t kI32Max = 2147483647;
@@ -115,6 +120,32 @@ int choose_bn(int64_t M, int64_t N, int sms, bool allow224) {
     return best;
 }
 
+// Split K for the dense GEMM: the number of K ranges S (1: none). Each
+// split unit ends with a partial-tile store, a GPU-scope fence, an arrival
+// count and (last unit) a read of the other partials, a few microseconds
+// during which the tile's MMA pipeline waits; so split K only pays where
+// few tiles run over a long K range. Measured on the B300 (K = 7168, 9
+// shapes from 256 x 576 to 2048 x 7168): the best S keeps about half the
+// co-resident units busy, S = round(slots / (2 units)), capped at 4; shapes
+// with more than ~slots / 3 tile units are fastest unsplit.
+int choose_splits(int64_t units, int64_t slots, int64_t KB) {
+    const int64_t kb4 = cdiv(KB, 4);
+    if (units <= 0 || kb4 < 2) return 1;
+    int64_t s = (slots + units) / (2 * units);  // round(slots / (2 units))
+    return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>({s, 4, kb4})));
+}
+
+// Workspace of a split-K call: S FP32 partial tiles of 128 rows x bn
+// columns for every output tile (m-tiles rounded up to pairs), then one
+// 32-bit arrival word per tile.
+size_t splitk_bytes(int64_t M, int64_t N, int splits, int bn) {
+    if (splits <= 1) return 0;
+    const int64_t tiles = 2 * cdiv(cdiv(M, 128), 2) * cdiv(N, bn);
+    const size_t part = static_cast<size_t>(splits) * tiles * bn * 128 * 4;
+    const size_t ctr = static_cast<size_t>(tiles) * 4;
+    return (part + 255) / 256 * 256 + (ctr + 255) / 256 * 256;
+}
+
 }  // namespace
 
 extern "C" {
@@ -139,6 +170,12 @@ void fp8q_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns = ns ? ns : 1000000000
 int fp8q_set_gemm_tile_n(int bn) {
     if (bn != 0 && bn != 128 && bn != 224 && bn != 256) return FP8Q_ERR_UNSUPPORTED;
     g_force_bn = bn;
+    return FP8Q_OK;
+}
+
+int fp8q_set_gemm_splits(int splits) {
+    if (splits < 0 || splits > kMaxSplits) return FP8Q_ERR_UNSUPPORTED;
+    g_force_splits = splits;
     return FP8Q_OK;
 }
 
@@ -313,18 +350,16 @@ namespace {
 
 // The dense GEMM C = A * B^T; row_scaled_b selects sb [N][KB] (one scale per
 // row of B) instead of sb [ceil(N/128)][KB].
-int dense_gemm(const void* A, const float* sa, const void* B, const float* sb, void* C_bf16,
-               int64_t M, int64_t N, int64_t K, bool row_scaled_b, cudaStream_t stream) {
-    if (M < 0 || N <= 0 || K <= 0 || M > kI32Max || N > kI32Max || K > kI32Max)
-        return FP8Q_ERR_SHAPE;
-    if (M == 0) return FP8Q_OK;
-    if (!A || !sa || !B || !sb || !C_bf16) return FP8Q_ERR_NULL;
-    if (K % 16 != 0 || N % 8 != 0 || !aligned(A, 16) || !aligned(B, 16) || !aligned(C_bf16, 16) ||
-        !aligned(sa, 4) || !aligned(sb, 4))
-        return FP8Q_ERR_ALIGN;
-    DeviceInfo* dev = nullptr;
-    if (int rc = current_device(&dev)) return rc;
+// The tile width, pair mode and co-resident clusters of a dense GEMM call.
+struct DensePlan {
+    int bn;
+    bool pair;
+    int clusters;  // pair mode: co-resident 2-CTA clusters
+    int64_t units; // tile units (pairs of m-tiles in pair mode) x n-tiles
+    int64_t slots; // units that run at once
+};
 
+int plan_dense(DeviceInfo* dev, int64_t M, int64_t N, bool row_scaled_b, DensePlan* p) {
     // the 224-wide tile exists for block-scaled B only; a forced 224 runs the
     // row-scaled GEMM 256 wide
     int bn = g_force_bn ? g_force_bn : choose_bn(M, N, dev->sms, !row_scaled_b);
@@ -337,6 +372,41 @@ int dense_gemm(const void* A, const float* sa, const void* B, const float* sb, v
         std::lock_guard<std::mutex> lock(g_mutex);
         if (*pc < 0) *pc = fp8q::gemm_pair_max_clusters(bn, row_scaled_b);
         pair = *pc > 0;
+    }
+    p->bn = bn;
+    p->pair = pair;
+    p->clusters = pair ? *pc : 0;
+    const int64_t mt = cdiv(M, 128);
+    p->units = (pair ? cdiv(mt, 2) : mt) * cdiv(N, bn);
+    p->slots = pair ? *pc : dev->sms;
+    return FP8Q_OK;
+}
+
+int dense_gemm(const void* A, const float* sa, const void* B, const float* sb, void* C_bf16,
+               int64_t M, int64_t N, int64_t K, bool row_scaled_b, void* workspace, size_t workspace_bytes,
+               cudaStream_t stream) {
+    if (M < 0 || N <= 0 || K <= 0 || M > kI32Max || N > kI32Max || K > kI32Max)
+        return FP8Q_ERR_SHAPE;
+    if (M == 0) return FP8Q_OK;
+    if (!A || !sa || !B || !sb || !C_bf16) return FP8Q_ERR_NULL;
+    if (K % 16 != 0 || N % 8 != 0 || !aligned(A, 16) || !aligned(B, 16) || !aligned(C_bf16, 16) ||
+        !aligned(sa, 4) || !aligned(sb, 4))
+        return FP8Q_ERR_ALIGN;
+    if (workspace && !aligned(workspace, 256)) return FP8Q_ERR_ALIGN;
+    DeviceInfo* dev = nullptr;
+    if (int rc = current_device(&dev)) return rc;
+    DensePlan plan;
+    plan_dense(dev, M, N, row_scaled_b, &plan);
+    const int bn = plan.bn;
+    const bool pair = plan.pair;
+    // split K only with a workspace (block-scaled B): the requested or chosen
+    // count, reduced until the workspace holds it
+    int splits = 1;
+    if (workspace && !row_scaled_b) {
+        splits = g_force_splits ? g_force_splits
+                                : choose_splits(plan.units, plan.slots, cdiv(K, 128));
+        splits = static_cast<int>(std::min<int64_t>(splits, cdiv(cdiv(K, 128), 4)));
+        while (splits > 1 && splitk_bytes(M, N, splits, bn) > workspace_bytes) --splits;
     }
     CUtensorMap tmA, tmB, tmC;
     if (!make_map_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, K, M, 128, 128) ||
@@ -370,14 +440,23 @@ int dense_gemm(const void* A, const float* sa, const void* B, const float* sb, v
     a.mt_count = static_cast<int32_t>(cdiv(M, 128));
     a.nt_count = static_cast<int32_t>(cdiv(N, bn));
     a.mp_count = static_cast<int32_t>(cdiv(a.mt_count, 2));
-    // work units: tiles, or pairs of m-tiles in pair mode
-    const int64_t units = static_cast<int64_t>(pair ? a.mp_count : a.mt_count) * a.nt_count;
+    // work units: tiles, or pairs of m-tiles in pair mode, times K ranges
+    const int64_t units = static_cast<int64_t>(pair ? a.mp_count : a.mt_count) * a.nt_count * splits;
     if (units > kI32Max) return FP8Q_ERR_SHAPE;
     a.num_tiles = static_cast<int32_t>(units);
+    a.splits = splits;
+    a.tile_units = static_cast<int32_t>(units / splits);
+    if (splits > 1) {
+        a.ws = static_cast<float*>(workspace);
+        const int64_t tiles = 2 * cdiv(cdiv(M, 128), 2) * cdiv(N, bn);
+        const size_t part = static_cast<size_t>(splits) * tiles * bn * 128 * 4;
+        a.counters = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + (part + 255) / 256 * 256);
+        a.epoch = g_epoch.fetch_add(1) % 0xFFFFFFu + 1u;
+    }
     a.timeout_ns = g_timeout_ns;
     a.debug = g_inject;
     if (pair) {
-        const int64_t clusters = units < *pc ? units : *pc;
+        const int64_t clusters = units < plan.clusters ? units : plan.clusters;
         g.grid = static_cast<unsigned>(2 * clusters);
     } else {
         g.grid = static_cast<unsigned>(units < dev->sms ? units : dev->sms);
@@ -391,12 +470,33 @@ extern "C" {
 
 int fp8_block_gemm(const void* A, const float* sa, const void* B, const float* sb, void* C_bf16,
                    int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
-    return dense_gemm(A, sa, B, sb, C_bf16, M, N, K, false, stream);
+    return dense_gemm(A, sa, B, sb, C_bf16, M, N, K, false, nullptr, 0, stream);
+}
+
+int fp8_block_gemm_workspace_size(int64_t M, int64_t N, int64_t K, size_t* bytes) {
+    if (!bytes) return FP8Q_ERR_NULL;
+    *bytes = 0;
+    if (M < 0 || N <= 0 || K <= 0 || M > kI32Max || N > kI32Max || K > kI32Max) return FP8Q_ERR_SHAPE;
+    if (M == 0) return FP8Q_OK;
+    DeviceInfo* dev = nullptr;
+    if (int rc = current_device(&dev)) return rc;
+    DensePlan plan;
+    plan_dense(dev, M, N, false, &plan);
+    int splits = g_force_splits ? g_force_splits : choose_splits(plan.units, plan.slots, cdiv(K, 128));
+    splits = static_cast<int>(std::min<int64_t>(splits, cdiv(cdiv(K, 128), 4)));
+    *bytes = splitk_bytes(M, N, splits, plan.bn);
+    return FP8Q_OK;
+}
+
+int fp8_block_gemm_ws(const void* A, const float* sa, const void* B, const float* sb, void* C_bf16,
+                      int64_t M, int64_t N, int64_t K, void* workspace, size_t workspace_bytes,
+                      cudaStream_t stream) {
+    return dense_gemm(A, sa, B, sb, C_bf16, M, N, K, false, workspace, workspace_bytes, stream);
 }
 
 int fp8_wgrad_gemm(const void* A, const float* sa, const void* B, const float* sb, void* C_bf16,
                    int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
-    return dense_gemm(A, sa, B, sb, C_bf16, M, N, K, true, stream);
+    return dense_gemm(A, sa, B, sb, C_bf16, M, N, K, true, nullptr, 0, stream);
 }
 
 }  // extern "C"

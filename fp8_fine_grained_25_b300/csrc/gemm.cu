@@ -109,8 +109,9 @@ struct Layout {
     // scale_full[slots], scale_empty[slots], drain
     static constexpr int FULL = 0, EMPTY = STAGES, TFULL = 2 * STAGES, TEMPTY = TFULL + NBUF,
                          SFULL = TEMPTY + NBUF, SEMPTY = SFULL + kScaleSlots,
-                         DRAIN = SEMPTY + kScaleSlots, NUM_BARS = DRAIN + 1;
-    static constexpr int MISC_OFF = BAR_OFF + 8 * NUM_BARS;  // tmem slot, abort flag
+                         DRAIN = SEMPTY + kScaleSlots, PARTIAL = DRAIN + 1, DECIDED = PARTIAL + 1,
+                         NUM_BARS = DECIDED + 1;
+    static constexpr int MISC_OFF = BAR_OFF + 8 * NUM_BARS;  // tmem slot, abort flag, last-split flag
     static constexpr int TABLE_OFF = MISC_OFF + 16;
     static constexpr int HALF = BN / 2;       // columns per promotion warp
     static constexpr int CHUNKS = HALF / 32;  // 32-column TMEM loads, issued in pairs
@@ -139,16 +140,34 @@ struct Tile {
     int n0;       // first column of C (= row of the expert's B)
     int brow;     // B row coordinate in the 2-D B tensor ([E*N, K] when grouped)
     int e;        // expert (0 when dense)
+    int kbeg, kend;  // this unit's K blocks (the whole K range unless split)
+    int ksplit;      // which K range (0 unless split)
 };
+
+// First K block of K range s of `splits` (ranges start on multiples of 4 K
+// blocks, the granularity of the scale ring).
+__device__ __forceinline__ int split_kbeg(int s, int splits, int KB) {
+    const int kb4 = (KB + 3) / 4;
+    return min(KB, 4 * ((s * kb4) / splits));
+}
 
 // Work unit t -> tile. Dense: groups of kGroupM row-units share n-tiles
 // for L2 reuse. Pair mode: a unit is a pair of m-tiles (2u, 2u + 1), CTA
 // `rank` of the pair takes m-tile 2u + rank and B rows n0 + rank * BN / 2.
-template <int BN, bool GROUPED, bool PAIR>
+template <int BN, bool GROUPED, bool PAIR, bool SPLITK = false>
 __device__ __forceinline__ Tile decode_tile(const GemmArgs& a, const int* table, int t,
                                             uint32_t rank) {
     Tile r;
+    r.kbeg = 0;
+    r.kend = a.KB;
+    r.ksplit = 0;
     if constexpr (!GROUPED) {
+        if constexpr (SPLITK) {  // split index slowest: a wave holds one K range of many tiles
+            r.ksplit = t / a.tile_units;
+            t -= r.ksplit * a.tile_units;
+            r.kbeg = split_kbeg(r.ksplit, a.splits, a.KB);
+            r.kend = split_kbeg(r.ksplit + 1, a.splits, a.KB);
+        }
         const int rows = PAIR ? a.mp_count : a.mt_count;
         const int per_group = kGroupM * a.nt_count;
         const int g = t / per_group, in = t - g * per_group;
@@ -258,7 +277,116 @@ __device__ __forceinline__ void promote_odd(float (&acc)[HALF], uint32_t taddr, 
     fma_cols<HALF - 16, 16>(acc, r3, o16 < split ? cs : csn);
 }
 
-template <int BN, bool GROUPED, bool PAIR, bool ROWB>
+// Column of this warp's tile slice that acc[i] holds: i itself, except for
+// 112-column warps (224-wide tiles), whose chunk order puts warp columns
+// 16 h .. 16 h + 95 in acc[0, 96) and the remaining 16 columns in acc[96, 112).
+template <int HALF>
+__device__ __forceinline__ int acc_col(int i, int h) {
+    if constexpr (HALF % 32 == 0) {
+        return i;
+    } else {
+        return i < HALF - 16 ? 16 * h + i : (HALF - 16) * (1 - h) + (i - (HALF - 16));
+    }
+}
+
+// One arrival on a tile's arrival word, tagged with this call's epoch: a word
+// holding another call's tag counts as zero. Returns the number of arrivals
+// of this call including this one (0 if the bounded retry loop gave up).
+__device__ __forceinline__ uint32_t arrive_count(uint32_t* word, uint32_t epoch, volatile int* abort_flag) {
+    uint32_t cur = *reinterpret_cast<volatile uint32_t*>(word);
+    for (int it = 0; it < (1 << 16); ++it) {
+        const uint32_t next = (cur >> 8) == epoch ? cur + 1u : ((epoch << 8) | 1u);
+        const uint32_t prev = atomicCAS(word, cur, next);
+        if (prev == cur) return next & 0xFFu;
+        cur = prev;
+    }
+    *abort_flag = 1;
+    return 0;
+}
+
+// Release / acquire fences at GPU scope (lighter than a sequentially
+// consistent fence): the partial tile's stores before the arrival count,
+// the arrival count before the other units' partials are read.
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+// Split K: write this unit's FP32 partial tile to the workspace, count the
+// unit's arrival on the tile's word, and if it is the last unit of the tile,
+// replace acc by the sum of all partials taken in range order (its own from
+// registers), so that C does not depend on which unit finishes last.
+// Workspace layout per K range and tile: [BN / 4 column groups][128 rows]
+// of float4, so a warp (32 consecutive rows) moves 512 contiguous bytes per
+// column group; tiles = m-tiles (rounded up to pairs in pair mode) x n-tiles,
+// and columns past N / rows past M hold unused values. The 8 promotion warps
+// meet on two barriers with bounded waits. Returns false if a wait gave up.
+template <int BN, bool PAIR, int HALF>
+__device__ __forceinline__ bool split_reduce(const GemmArgs& a, const Tile& tile, float (&acc)[HALF],
+                                             int row, int h, int ew, int lane, uint32_t bar_partial,
+                                             uint32_t bar_decided, uint32_t phase, volatile uint32_t* last_flag,
+                                             volatile int* abort_flag, uint64_t limit, bool& last) {
+    const int64_t tiles = static_cast<int64_t>(PAIR ? 2 * a.mp_count : a.mt_count) * a.nt_count;
+    const int64_t ctile = static_cast<int64_t>(tile.m0 / BM) * a.nt_count + tile.n0 / BN;
+    const int64_t range_f4 = tiles * (BN / 4) * BM;  // float4s per K range
+    // this row's float4 in column group 0 of this warp's slice, K range 0;
+    // column group g is g * 128 float4s further
+    const float4* base = reinterpret_cast<const float4*>(a.ws) + ctile * (BN / 4) * BM + (h * HALF / 4) * BM + row;
+    float4* mine = const_cast<float4*>(base) + tile.ksplit * range_f4;
+#pragma unroll
+    for (int i = 0; i < HALF; i += 4)
+        __stcg(mine + (acc_col<HALF>(i, h) / 4) * BM, make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]));
+    fence_acq_rel_gpu();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_partial);
+    if (ew == 0) {
+        if (!warp_wait(bar_partial, phase, abort_flag, limit)) return false;
+        if (lane == 0) {
+            const uint32_t n = arrive_count(a.counters + ctile, a.epoch, abort_flag);
+            fence_acq_rel_gpu();
+            *last_flag = n == static_cast<uint32_t>(a.splits) ? 1u : 0u;
+            mbar_arrive(bar_decided);
+        }
+        __syncwarp();
+    }
+    if (!warp_wait(bar_decided, phase, abort_flag, limit)) return false;
+    last = *last_flag != 0u;
+    if (!last) return true;
+    fence_acq_rel_gpu();
+    // 16 columns at a time, all loads of one K range issued together:
+    // (p_0 + ... + p_(me-1)) + acc, then + p_(me+1) + ... (range order)
+    const int me = tile.ksplit;
+#pragma unroll
+    for (int i0 = 0; i0 < HALF; i0 += 16) {
+        const float4* b = base + (acc_col<HALF>(i0, h) / 4) * BM;
+        float* c = acc + i0;
+        if (me > 0) {
+            float4 r0 = __ldcg(b), r1 = __ldcg(b + BM), r2 = __ldcg(b + 2 * BM), r3 = __ldcg(b + 3 * BM);
+            for (int s = 1; s < me; ++s) {
+                const float4* q = b + s * range_f4;
+                const float4 p0 = __ldcg(q), p1 = __ldcg(q + BM), p2 = __ldcg(q + 2 * BM), p3 = __ldcg(q + 3 * BM);
+                r0.x += p0.x; r0.y += p0.y; r0.z += p0.z; r0.w += p0.w;
+                r1.x += p1.x; r1.y += p1.y; r1.z += p1.z; r1.w += p1.w;
+                r2.x += p2.x; r2.y += p2.y; r2.z += p2.z; r2.w += p2.w;
+                r3.x += p3.x; r3.y += p3.y; r3.z += p3.z; r3.w += p3.w;
+            }
+            c[0] = r0.x + c[0]; c[1] = r0.y + c[1]; c[2] = r0.z + c[2]; c[3] = r0.w + c[3];
+            c[4] = r1.x + c[4]; c[5] = r1.y + c[5]; c[6] = r1.z + c[6]; c[7] = r1.w + c[7];
+            c[8] = r2.x + c[8]; c[9] = r2.y + c[9]; c[10] = r2.z + c[10]; c[11] = r2.w + c[11];
+            c[12] = r3.x + c[12]; c[13] = r3.y + c[13]; c[14] = r3.z + c[14]; c[15] = r3.w + c[15];
+        }
+        for (int s = me + 1; s < a.splits; ++s) {
+            const float4* q = b + s * range_f4;
+            const float4 p0 = __ldcg(q), p1 = __ldcg(q + BM), p2 = __ldcg(q + 2 * BM), p3 = __ldcg(q + 3 * BM);
+            c[0] += p0.x; c[1] += p0.y; c[2] += p0.z; c[3] += p0.w;
+            c[4] += p1.x; c[5] += p1.y; c[6] += p1.z; c[7] += p1.w;
+            c[8] += p2.x; c[9] += p2.y; c[10] += p2.z; c[11] += p2.w;
+            c[12] += p3.x; c[13] += p3.y; c[14] += p3.z; c[15] += p3.w;
+        }
+    }
+    return true;
+}
+
+// SPLITK: work units are (tile, K range) pairs and the epilogue reduces the
+// partial tiles through the workspace (dense block-scaled GEMM only).
+template <int BN, bool GROUPED, bool PAIR, bool ROWB, bool SPLITK>
 __global__ void __launch_bounds__(kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
@@ -300,6 +428,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(L::SEMPTY + j), kEpiWarps);
         }
         mbar_init(bar(L::DRAIN), 1);
+        mbar_init(bar(L::PARTIAL), kEpiWarps);
+        mbar_init(bar(L::DECIDED), 1);
         *abort_flag = 0;
         fence_barrier_init();
         fence_proxy_async_smem();
@@ -337,8 +467,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0, issued = 0;
             bool ok = true;
             for (int t = unit0; ok && t < num_tiles; t += unit_step) {
-                const Tile tile = decode_tile<BN, GROUPED, PAIR>(args, table, t, rank);
-                for (int kb = 0; kb < KB; ++kb) {
+                const Tile tile = decode_tile<BN, GROUPED, PAIR, SPLITK>(args, table, t, rank);
+                for (int kb = tile.kbeg; kb < tile.kend; ++kb) {
                     if (!warp_wait(bar(L::EMPTY + stage), phase ^ 1u, abort_flag, limit)) {
                         ok = false;
                         break;
@@ -383,7 +513,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0, abuf = 0, aphase = 0;
             bool ok = true, issued_any = false;
             for (int t = unit0; ok && t < num_tiles; t += unit_step) {
-                for (int kb = 0; kb < KB; ++kb) {
+                const Tile tile = decode_tile<BN, GROUPED, PAIR, SPLITK>(args, table, t, rank);
+                for (int kb = tile.kbeg; kb < tile.kend; ++kb) {
                     // the operands usually land long before the accumulator
                     // buffer is released: wait for them first, so that only
                     // the release stands between the promotion and the MMA
@@ -452,11 +583,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t sphase = 0;
             bool ok = true;
             for (int t = unit0; ok && t < num_tiles; t += unit_step) {
-                const Tile tile = decode_tile<BN, GROUPED, PAIR>(args, table, t, rank);
+                const Tile tile = decode_tile<BN, GROUPED, PAIR, SPLITK>(args, table, t, rank);
                 const float* sb_e = args.sb + static_cast<int64_t>(tile.e) * args.NB * KB;
                 const int nb = (tile.n0 >> 7) + (lane < L::MAX_NB ? lane : 0);
                 const bool sb_ok = lane < L::MAX_NB && nb < args.NB && (nb << 7) < tile.n0 + BN;
-                for (int kb0 = 0; kb0 < KB; kb0 += kScaleKb) {
+                for (int kb0 = tile.kbeg; kb0 < tile.kend; kb0 += kScaleKb) {
                     if (!warp_wait(bar(L::SEMPTY + slot), sphase ^ 1u, abort_flag, limit)) {
                         ok = false;
                         break;
@@ -529,10 +660,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         int slot = 0;
         uint32_t sphase = 0;
         uint32_t ebox = 0;  // epilogue boxes staged so far: their buffer alternates
+        uint32_t sred_phase = 0;  // split-K reductions done so far (barrier parity)
         bool ok = true;
         const uint32_t temptry_base = PAIR ? mapa_shared(bar(L::TEMPTY), 0) : bar(L::TEMPTY);
         for (int t = unit0; ok && t < num_tiles; t += unit_step) {
-            const Tile tile = decode_tile<BN, GROUPED, PAIR>(args, table, t, rank);
+            const Tile tile = decode_tile<BN, GROUPED, PAIR, SPLITK>(args, table, t, rank);
             const int m = tile.m0 + row;
             const bool row_ok = m < tile.row_end;
             const int col0 = tile.n0 + h * L::HALF;  // first column of this warp
@@ -550,7 +682,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int split = 128 - (wcol & 127);
             float4 sa4 = make_float4(0.f, 0.f, 0.f, 0.f), sb4 = sa4, sb4n = sa4;
             const float* sb_cols = scale_ring;  // ROWB: this warp's sb columns in the slot
-            for (int kb = 0; kb < KB; ++kb) {
+            for (int kb = tile.kbeg; kb < tile.kend; ++kb) {
                 const int j = kb & (kScaleKb - 1);
                 if (j == 0) {
                     // scales of K blocks kb .. kb + 3, from the ring (staged ahead)
@@ -632,7 +764,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     else mbar_arrive(bar(L::TEMPTY + abuf));
                 }
                 if constexpr (ROWB) {
-                    if (j == kScaleKb - 1 || kb == KB - 1) {
+                    if (j == kScaleKb - 1 || kb == tile.kend - 1) {
                         if (lane == 0) mbar_arrive(bar(L::SEMPTY + slot));
                         if (++slot == kScaleSlots) {
                             slot = 0;
@@ -646,6 +778,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (!ok) break;
+
+            if constexpr (SPLITK) {
+                {
+                    bool last = false;
+                    if (!split_reduce<BN, PAIR, L::HALF>(args, tile, acc, row, h, ew, lane,
+                                               bar(L::PARTIAL), bar(L::DECIDED), sred_phase,
+                                               reinterpret_cast<volatile uint32_t*>(smem + L::MISC_OFF + 8),
+                                               abort_flag, limit, last)) {
+                        ok = false;
+                        break;
+                    }
+                    sred_phase ^= 1u;
+                    if (!last) continue;  // another unit of this tile stores C
+                }
+            }
 
             if constexpr (!GROUPED) {
                 // bf16 -> swizzled staging (32 rows x EPI_BOX_COLS per box, two
@@ -727,9 +874,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0 && *abort_flag) atomicOr(&g_device_status, FP8Q_DEVSTATUS_TIMEOUT);
 }
 
-template <int BN, bool GROUPED, bool PAIR, bool ROWB>
+template <int BN, bool GROUPED, bool PAIR, bool ROWB, bool SPLITK = false>
 cudaError_t prepare(int smem) {
-    auto kern = fp8_gemm_kernel<BN, GROUPED, PAIR, ROWB>;
+    auto kern = fp8_gemm_kernel<BN, GROUPED, PAIR, ROWB, SPLITK>;
     // setmaxnreg.inc waits until the registers it asks for are free in the
     // CTA's launch pool; a pool smaller than the split would never satisfy
     // it, so refuse to launch in that case.
@@ -741,12 +888,12 @@ cudaError_t prepare(int smem) {
     return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
 }
 
-template <int BN, bool GROUPED, bool PAIR, bool ROWB = false>
+template <int BN, bool GROUPED, bool PAIR, bool ROWB = false, bool SPLITK = false>
 cudaError_t launch_one(const GemmLaunch& g) {
     using L = Layout<BN, GROUPED, PAIR, ROWB>;
-    auto kern = fp8_gemm_kernel<BN, GROUPED, PAIR, ROWB>;
+    auto kern = fp8_gemm_kernel<BN, GROUPED, PAIR, ROWB, SPLITK>;
     const int smem = L::smem_bytes(GROUPED ? g.args.E : 0);
-    cudaError_t err = prepare<BN, GROUPED, PAIR, ROWB>(smem);
+    cudaError_t err = prepare<BN, GROUPED, PAIR, ROWB, SPLITK>(smem);
     if (err != cudaSuccess) return err;
     if constexpr (!PAIR) {
         kern<<<g.grid, kThreads, smem, g.stream>>>(*g.tmA, *g.tmB, *g.tmC, g.args);
@@ -785,7 +932,7 @@ int pair_max_clusters() {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, fp8_gemm_kernel<BN, false, true, ROWB>, &cfg) != cudaSuccess)
+    if (cudaOccupancyMaxActiveClusters(&n, fp8_gemm_kernel<BN, false, true, ROWB, false>, &cfg) != cudaSuccess)
         return 0;
     return n;
 }
@@ -837,6 +984,21 @@ cudaError_t launch_gemm(const GemmLaunch& g) {
         switch (g.bn) {
             case 128: return launch_one<128, false, false, true>(g);
             case 256: return launch_one<256, false, false, true>(g);
+        }
+    } else if (g.args.splits > 1) {
+        // split K: the same tile widths with the partial-tile epilogue
+        if (g.pair) {
+            switch (g.bn) {
+                case 128: return launch_one<128, false, true, false, true>(g);
+                case 224: return launch_one<224, false, true, false, true>(g);
+                case 256: return launch_one<256, false, true, false, true>(g);
+            }
+        } else {
+            switch (g.bn) {
+                case 128: return launch_one<128, false, false, false, true>(g);
+                case 224: return launch_one<224, false, false, false, true>(g);
+                case 256: return launch_one<256, false, false, false, true>(g);
+            }
         }
     } else if (g.pair) {
         switch (g.bn) {

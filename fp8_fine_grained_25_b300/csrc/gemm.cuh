@@ -20,7 +20,16 @@ struct GemmArgs {
     int32_t E;               // experts (grouped), else 1
     int32_t mt_count, nt_count;
     int32_t mp_count;        // pair mode: ceil(mt_count / 2) row units
-    int32_t num_tiles;       // dense only; the grouped kernel counts its own
+    int32_t num_tiles;       // dense only (tile units x splits); the grouped kernel counts its own
+    // Split K (dense block-scaled GEMM only): each tile's K blocks are cut
+    // into `splits` ranges (multiples of 4 K blocks) computed by different
+    // work units; every unit writes its FP32 partial tile to ws, and the last
+    // unit of a tile to arrive sums the partials in split order and stores C.
+    int32_t splits;          // 1: no split
+    int32_t tile_units;      // work units per split (num_tiles = tile_units * splits)
+    float* ws;               // splits > 1: FP32 partial tiles [splits][M][N]
+    uint32_t* counters;      // splits > 1: one arrival word per 128-row x BN tile
+    uint32_t epoch;          // splits > 1: this call's tag in the arrival words (1 .. 2^24 - 1)
     uint64_t timeout_ns;
     uint32_t debug;          // FP8Q_INJECT_STALLED_STAGE: first pipeline stage never completes
 };

@@ -28,6 +28,10 @@ lib.fp8q_quant_act_ue8m0.argtypes = [_p, _i64, _i64, _p, _p, _p]
 lib.fp8q_quant_weight_ue8m0.argtypes = [_p, _i64, _i64, _p, _p, _p]
 lib.fp8q_quant_weight_t.argtypes = [_p, _i64, _i64, _p, _p, _p, _p, _p]
 lib.fp8_block_gemm.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p]
+lib.fp8_block_gemm_ws.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p, ctypes.c_size_t, _p]
+lib.fp8_block_gemm_workspace_size.argtypes = [_i64, _i64, _i64, ctypes.POINTER(ctypes.c_size_t)]
+lib.fp8q_set_gemm_splits.argtypes = [ctypes.c_int]
+lib.fp8q_set_gemm_splits.restype = ctypes.c_int
 lib.fp8_wgrad_gemm.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p]
 lib.fp8_block_gemm_ue8m0.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p]
 lib.fp8_wgrad_gemm_ue8m0.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p]
@@ -49,7 +53,8 @@ lib.fp8q_status_string.argtypes = [ctypes.c_int]
 lib.fp8q_status_string.restype = ctypes.c_char_p
 for _f in ("fp8q_quant_act", "fp8q_quant_weight", "fp8q_quant_act_t", "fp8q_quant_weight_t",
            "fp8q_quant_act_ue8m0", "fp8q_quant_weight_ue8m0",
-           "fp8_block_gemm", "fp8_wgrad_gemm", "fp8_block_gemm_ue8m0", "fp8_wgrad_gemm_ue8m0",
+           "fp8_block_gemm", "fp8_block_gemm_ws", "fp8_block_gemm_workspace_size",
+           "fp8_wgrad_gemm", "fp8_block_gemm_ue8m0", "fp8_wgrad_gemm_ue8m0",
            "fp8q_quant_act_t_ue8m0", "fp8q_quant_weight_t_ue8m0", "fp8_grouped_gemm",
            "fp8q_get_device_status"):
     getattr(lib, _f).restype = ctypes.c_int
@@ -307,6 +312,40 @@ def fp8_block_gemm(A: torch.Tensor, sa: torch.Tensor, B: torch.Tensor, sb: torch
     return C
 
 
+def fp8_block_gemm_workspace_size(M: int, N: int, K: int) -> int:
+    """Bytes of workspace fp8_block_gemm_ws uses for an M x N x K call on the
+    current device (0: it would not split K)."""
+    n = ctypes.c_size_t(0)
+    _check(lib.fp8_block_gemm_workspace_size(int(M), int(N), int(K), ctypes.byref(n)),
+           "fp8_block_gemm_workspace_size")
+    return int(n.value)
+
+
+def fp8_block_gemm_ws(A: torch.Tensor, sa: torch.Tensor, B: torch.Tensor, sb: torch.Tensor,
+                      C: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                      stream=None) -> torch.Tensor:
+    """fp8_block_gemm with split K through a caller-owned workspace (a uint8
+    CUDA tensor; allocated here at the size fp8_block_gemm_workspace_size
+    gives when not passed)."""
+    M, K = A.shape
+    N = B.shape[0]
+    _need(A, "A", CODE_DTYPES, (M, K))
+    _need(B, "B", CODE_DTYPES, (N, K))
+    _need(sa, "sa", (torch.float32,), (M, _cdiv(K, 128)))
+    _need(sb, "sb", (torch.float32,), (_cdiv(N, 128), _cdiv(K, 128)))
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    _need(C, "C", (torch.bfloat16,), (M, N))
+    if workspace is None:
+        workspace = torch.empty(max(256, fp8_block_gemm_workspace_size(M, N, K)), dtype=torch.uint8,
+                                device=A.device)
+    _need(workspace, "workspace", (torch.uint8,), None)
+    _check(lib.fp8_block_gemm_ws(A.data_ptr(), sa.data_ptr(), B.data_ptr(), sb.data_ptr(), C.data_ptr(),
+                                 M, N, K, workspace.data_ptr(), workspace.numel(), _stream(stream)),
+           "fp8_block_gemm_ws")
+    return C
+
+
 def fp8_wgrad_gemm(A: torch.Tensor, sa: torch.Tensor, B: torch.Tensor, sb: torch.Tensor,
                    C: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """C[M, N] (bf16) = A[M, K] * B[N, K]^T with one scale per row of each
@@ -404,6 +443,11 @@ def fp8q_set_gemm_tile_n(bn: int) -> None:
     """Force the dense GEMM's output-tile width (128, 224 or 256; 0 = automatic;
     224 applies to the block-scaled GEMM, the weight-gradient GEMM runs 256)."""
     _check(lib.fp8q_set_gemm_tile_n(int(bn)), "fp8q_set_gemm_tile_n")
+
+
+def fp8q_set_gemm_splits(splits: int) -> None:
+    """Force the number of K ranges of fp8_block_gemm_ws (1 .. 8; 0 = automatic)."""
+    _check(lib.fp8q_set_gemm_splits(int(splits)), "fp8q_set_gemm_splits")
 
 
 def fp8q_set_gemm_pairs(enable: bool) -> None:

@@ -39,6 +39,7 @@
 #ifndef FP8Q_H
 #define FP8Q_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -182,6 +183,41 @@ FP8Q_API int fp8_block_gemm(const void* A, const float* sa, const void* B, const
                    int64_t M, int64_t N, int64_t K, cudaStream_t stream);
 
 /*
+ * fp8_block_gemm with split K, for shapes whose output tiles fill few waves
+ * of the 148 SMs (the MLA down-projections of the news.qq.com page's
+ * "Multi-head Latent Attention" section: N = 1536 and 576 at M = 4096).
+ * The K blocks of each output tile are cut into S ranges (multiples of 4
+ * K blocks) computed by different work units; each unit writes its FP32
+ * partial tile into the workspace, and the last unit of a tile to finish
+ * adds the S partials in range order and stores C. The result does not
+ * depend on which unit finishes last, and differs from fp8_block_gemm only
+ * by the order of the FP32 additions (within the same accuracy bound).
+ *   workspace      in/out: DEVICE memory owned by the caller, 256-byte
+ *                  aligned, of workspace_bytes bytes; it needs no
+ *                  initialisation and keeps no state a later call relies on
+ *                  (arrival words are tagged with a per-call number).
+ *   workspace_bytes: the library uses the S it would pick for the shape (or
+ *                  the one set by fp8q_set_gemm_splits), reduced until
+ *                  S x M x N x 4 bytes of partials plus one 4-byte word per
+ *                  128 x tile-width output tile fit; S = 1 (no workspace
+ *                  used) is plain fp8_block_gemm. workspace may be NULL
+ *                  (then S = 1).
+ * Calls that share a workspace must not run concurrently (e.g. on two
+ * streams). Other arguments, alignment rules and errors as fp8_block_gemm;
+ * FP8Q_ERR_ALIGN also for a workspace not 256-byte aligned.
+ */
+FP8Q_API int fp8_block_gemm_ws(const void* A, const float* sa, const void* B, const float* sb,
+                               void* C_bf16, int64_t M, int64_t N, int64_t K, void* workspace,
+                               size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Bytes of workspace fp8_block_gemm_ws would use for an M x N x K call on
+ * the current device with the current settings (0: it would not split K).
+ * Returns FP8Q_OK, FP8Q_ERR_NULL, FP8Q_ERR_SHAPE or a device error.
+ */
+FP8Q_API int fp8_block_gemm_workspace_size(int64_t M, int64_t N, int64_t K, size_t* bytes);
+
+/*
  * The block-scaled FP8 GEMM with power-of-two (UE8M0) scales from
  * fp8q_quant_act_ue8m0 / fp8q_quant_weight_ue8m0 (a variant the pages do not
  * describe). The tensor core applies the scales itself (block-scaled MMA,
@@ -284,6 +320,14 @@ FP8Q_API void fp8q_set_wait_timeout_ns(uint64_t ns);
  * only, never results. Returns FP8Q_ERR_UNSUPPORTED for other values.
  */
 FP8Q_API int fp8q_set_gemm_tile_n(int bn);
+
+/*
+ * Number of K ranges fp8_block_gemm_ws splits each output tile into: 1 .. 8,
+ * or 0 (the default) to let the library pick per shape (still capped by the
+ * workspace and by one range per 4 K blocks). Affects speed and the order
+ * of FP32 additions only. Returns FP8Q_ERR_UNSUPPORTED for other values.
+ */
+FP8Q_API int fp8q_set_gemm_splits(int splits);
 
 /*
  * Whether fp8_block_gemm, fp8_wgrad_gemm and fp8_block_gemm_ue8m0 may run an output tile of

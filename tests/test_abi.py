@@ -213,3 +213,37 @@ def test_tile_width_setter(lib):
     for bn in (64, 160, 192, 512, -1):
         assert lib.fp8q_set_gemm_tile_n(bn) == UNSUPPORTED, bn
     assert lib.fp8q_set_gemm_tile_n(0) == OK
+
+
+def _gws(lib, *a):
+    f = lib.fp8_block_gemm_ws
+    f.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int64] * 3 + [ctypes.c_void_p, ctypes.c_size_t,
+                                                                 ctypes.c_void_p]
+    return f(*a)
+
+
+def test_split_k_gemm_argument_checks(lib):
+    # the same host checks as fp8_block_gemm, made before any device call
+    assert _gws(lib, P, P, P, P, P, -1, 256, 512, P, 1 << 20, None) == SHAPE
+    assert _gws(lib, None, None, None, None, None, 0, 256, 512, None, 0, None) == OK
+    for i in range(5):
+        args = [P] * 5
+        args[i] = None
+        assert _gws(lib, *args, 128, 256, 512, P, 1 << 20, None) == NULL
+    assert _gws(lib, P, P, P, P, P, 128, 252, 512, P, 1 << 20, None) == ALIGN    # N % 8
+    assert _gws(lib, P, P, P, P, P, 128, 256, 512, P + 16, 1 << 20, None) == ALIGN  # workspace
+    f = lib.fp8_block_gemm_workspace_size
+    f.argtypes = [ctypes.c_int64] * 3 + [ctypes.POINTER(ctypes.c_size_t)]
+    n = ctypes.c_size_t(7)
+    assert f(128, 256, 512, None) == NULL
+    assert f(-1, 256, 512, ctypes.byref(n)) == SHAPE and n.value == 0
+    assert f(0, 256, 512, ctypes.byref(n)) == OK and n.value == 0
+
+
+def test_split_count_setter(lib):
+    OK, UNSUPPORTED = 0, 7
+    for s in range(0, 9):
+        assert lib.fp8q_set_gemm_splits(s) == OK, s
+    for s in (-1, 9, 64):
+        assert lib.fp8q_set_gemm_splits(s) == UNSUPPORTED, s
+    assert lib.fp8q_set_gemm_splits(0) == OK
