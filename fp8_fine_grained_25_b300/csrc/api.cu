@@ -604,3 +604,62 @@ int fp8_grouped_gemm(const void* A, const float* sa, const void* B, const float*
 }
 
 }  // extern "C"
+
+// ----------------------------------------------------------------------------
+// Split-K GEMM for callers that cannot allocate device memory.
+//
+// fp8_block_gemm_ws needs a workspace from its caller. Some callers have no
+// way to provide one: code that may not call cudaMalloc (which can
+// synchronise the device and is not allowed everywhere a GEMM is issued), or
+// a framework that hands a custom operation only its input and output
+// buffers. fp8_block_gemm_static runs the same split-K kernel with its
+// scratch in a fixed array that lives in this library's device image: every
+// GPU that loads the library holds FP8Q_STATIC_SCRATCH_BYTES for it until
+// the process exits, and no call allocates anything.
+static __device__ __align__(256) unsigned char g_static_scratch[FP8Q_STATIC_SCRATCH_BYTES];
+
+namespace {
+
+// Device address of g_static_scratch on each device; the host-side name is
+// only a stand-in and must never reach a kernel. Resolved on the first call
+// per device, under g_mutex.
+void* g_static_scratch_addr[kMaxDevices];
+
+}  // namespace
+
+extern "C" {
+
+int fp8_block_gemm_static(const void* A, const float* sa, const void* B, const float* sb, void* C_bf16,
+                          int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
+    if (M < 0 || N <= 0 || K <= 0 || M > kI32Max || N > kI32Max || K > kI32Max) return FP8Q_ERR_SHAPE;
+    if (M == 0) return FP8Q_OK;
+    if (!A || !sa || !B || !sb || !C_bf16) return FP8Q_ERR_NULL;
+    if (K % 16 != 0 || N % 8 != 0 || !aligned(A, 16) || !aligned(B, 16) || !aligned(C_bf16, 16) ||
+        !aligned(sa, 4) || !aligned(sb, 4))
+        return FP8Q_ERR_ALIGN;
+    DeviceInfo* dev = nullptr;
+    if (int rc = current_device(&dev)) return rc;
+    // the split count this call runs with, and the scratch it needs
+    DensePlan plan;
+    plan_dense(dev, M, N, false, &plan);
+    int splits = g_force_splits ? g_force_splits : choose_splits(plan.units, plan.slots, cdiv(K, 128));
+    splits = static_cast<int>(std::min<int64_t>(splits, cdiv(cdiv(K, 128), 4)));
+    const size_t need = splitk_bytes(M, N, splits, plan.bn);
+    if (need > FP8Q_STATIC_SCRATCH_BYTES) return FP8Q_ERR_SHAPE;
+    if (need == 0) return dense_gemm(A, sa, B, sb, C_bf16, M, N, K, false, nullptr, 0, stream);
+    int d = 0;
+    if (cudaGetDevice(&d) != cudaSuccess) return FP8Q_ERR_CUDA;
+    void* scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        if (!g_static_scratch_addr[d]) {
+            void* p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return FP8Q_ERR_CUDA;
+            g_static_scratch_addr[d] = p;
+        }
+        scratch = g_static_scratch_addr[d];
+    }
+    return dense_gemm(A, sa, B, sb, C_bf16, M, N, K, false, scratch, FP8Q_STATIC_SCRATCH_BYTES, stream);
+}
+
+}  // extern "C"

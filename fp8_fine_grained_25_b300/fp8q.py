@@ -30,6 +30,7 @@ lib.fp8q_quant_weight_t.argtypes = [_p, _i64, _i64, _p, _p, _p, _p, _p]
 lib.fp8_block_gemm.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p]
 lib.fp8_block_gemm_ws.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p, ctypes.c_size_t, _p]
 lib.fp8_block_gemm_workspace_size.argtypes = [_i64, _i64, _i64, ctypes.POINTER(ctypes.c_size_t)]
+lib.fp8_block_gemm_static.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p]
 lib.fp8q_set_gemm_splits.argtypes = [ctypes.c_int]
 lib.fp8q_set_gemm_splits.restype = ctypes.c_int
 lib.fp8_wgrad_gemm.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p]
@@ -53,7 +54,7 @@ lib.fp8q_status_string.argtypes = [ctypes.c_int]
 lib.fp8q_status_string.restype = ctypes.c_char_p
 for _f in ("fp8q_quant_act", "fp8q_quant_weight", "fp8q_quant_act_t", "fp8q_quant_weight_t",
            "fp8q_quant_act_ue8m0", "fp8q_quant_weight_ue8m0",
-           "fp8_block_gemm", "fp8_block_gemm_ws", "fp8_block_gemm_workspace_size",
+           "fp8_block_gemm", "fp8_block_gemm_ws", "fp8_block_gemm_workspace_size", "fp8_block_gemm_static",
            "fp8_wgrad_gemm", "fp8_block_gemm_ue8m0", "fp8_wgrad_gemm_ue8m0",
            "fp8q_quant_act_t_ue8m0", "fp8q_quant_weight_t_ue8m0", "fp8_grouped_gemm",
            "fp8q_get_device_status"):
@@ -343,6 +344,25 @@ def fp8_block_gemm_ws(A: torch.Tensor, sa: torch.Tensor, B: torch.Tensor, sb: to
     _check(lib.fp8_block_gemm_ws(A.data_ptr(), sa.data_ptr(), B.data_ptr(), sb.data_ptr(), C.data_ptr(),
                                  M, N, K, workspace.data_ptr(), workspace.numel(), _stream(stream)),
            "fp8_block_gemm_ws")
+    return C
+
+
+def fp8_block_gemm_static(A: torch.Tensor, sa: torch.Tensor, B: torch.Tensor, sb: torch.Tensor,
+                          C: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """fp8_block_gemm_ws with the library's built-in scratch array instead of a
+    workspace: for callers that cannot allocate device memory (the C entry
+    point allocates nothing; only C is allocated here when not passed)."""
+    M, K = A.shape
+    N = B.shape[0]
+    _need(A, "A", CODE_DTYPES, (M, K))
+    _need(B, "B", CODE_DTYPES, (N, K))
+    _need(sa, "sa", (torch.float32,), (M, _cdiv(K, 128)))
+    _need(sb, "sb", (torch.float32,), (_cdiv(N, 128), _cdiv(K, 128)))
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    _need(C, "C", (torch.bfloat16,), (M, N))
+    _check(lib.fp8_block_gemm_static(A.data_ptr(), sa.data_ptr(), B.data_ptr(), sb.data_ptr(), C.data_ptr(),
+                                     M, N, K, _stream(stream)), "fp8_block_gemm_static")
     return C
 
 

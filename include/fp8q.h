@@ -211,6 +211,34 @@ FP8Q_API int fp8_block_gemm_ws(const void* A, const float* sa, const void* B, co
                                size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * fp8_block_gemm_ws for callers that cannot allocate device memory. There is
+ * no counterpart of this call on the pages; it exists for code that may not
+ * call cudaMalloc where it issues the GEMM (cudaMalloc can synchronise the
+ * device), or that receives only its input and output buffers from a host
+ * framework. It runs the same split-K kernel, with its scratch in a fixed
+ * array inside the library's device image instead of a caller workspace:
+ *   - every GPU that loads the library holds FP8Q_STATIC_SCRATCH_BYTES
+ *     (32 MiB) of device memory for that array until the process exits;
+ *   - the call allocates nothing and frees nothing;
+ *   - a call whose split count (chosen per shape, or set with
+ *     fp8q_set_gemm_splits) needs more scratch than the array holds
+ *     (S x 128-row x tile-width FP32 partial tiles plus one 4-byte word per
+ *     tile; see fp8_block_gemm_workspace_size) returns FP8Q_ERR_SHAPE and
+ *     launches nothing; a shape that does not split runs as fp8_block_gemm;
+ *   - all calls in the process share the array, and it keeps whatever the
+ *     last call left in it. Nothing in it needs to start at zero (the
+ *     arrival words carry a per-call tag), but calls that overlap on the
+ *     GPU (two streams, or two host threads) race on it: serialise them;
+ *   - the first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before capturing the stream into a CUDA graph.
+ * Arguments, layouts, alignment, accuracy and other errors as fp8_block_gemm.
+ */
+#define FP8Q_STATIC_SCRATCH_BYTES (32u << 20)
+FP8Q_API int fp8_block_gemm_static(const void* A, const float* sa, const void* B, const float* sb,
+                                   void* C_bf16, int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+
+/*
  * Bytes of workspace fp8_block_gemm_ws would use for an M x N x K call on
  * the current device with the current settings (0: it would not split K).
  * Returns FP8Q_OK, FP8Q_ERR_NULL, FP8Q_ERR_SHAPE or a device error.

@@ -247,3 +247,12 @@ def test_split_count_setter(lib):
     for s in (-1, 9, 64):
         assert lib.fp8q_set_gemm_splits(s) == UNSUPPORTED, s
     assert lib.fp8q_set_gemm_splits(0) == OK
+
+
+def test_static_scratch_gemm_argument_checks(lib):
+    f = lib.fp8_block_gemm_static
+    f.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int64] * 3 + [ctypes.c_void_p]
+    assert f(P, P, P, P, P, -1, 256, 512, None) == SHAPE
+    assert f(None, None, None, None, None, 0, 256, 512, None) == OK
+    assert f(P, P, None, P, P, 128, 256, 512, None) == NULL
+    assert f(P, P, P, P, P, 128, 252, 512, None) == ALIGN
