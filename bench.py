@@ -830,6 +830,7 @@ def extra_legs(device, peaks):
         "hbm_frac": (wbytes + abytes) / t / 1e9 / peaks["hbm_gbs"],
         "roofline_ms": roof_t * 1e3, "frac_of_roofline": roof_t / t,
         "bytes_per_launch": wbytes + abytes, "flops_per_launch": fl,
+        "traffic_bytes_per_launch": profiled_traffic("gemm_grouped_moe.md", "gemm.cu"),
         "timed": "alone, back to back, mean of the middle 12 of 20 (weights 3.76 GB > L2)"}
     del qa, sa, qw, sw, C, w
     torch.cuda.empty_cache()
@@ -845,6 +846,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5, 6, 7, 8, 9, 10])
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--extras", choices=["all", "none"], default="all",
+                    help="none: skip the kernels timed at other shapes and the cuBLAS FP8 ceiling "
+                         "(for profiler runs)")
     ap.add_argument("--experts", type=int, default=0,
                     help="MoE configs: keep this many experts (same tokens per expert)")
     args = ap.parse_args()
@@ -927,9 +931,9 @@ def main():
     # FP8:BF16 ratio), in its burst form when the timed region is short and
     # ran without a power cap, else in its sustained form.
     extra = {}
-    if args.config == 3 and rank == 0 and world == 1:
+    if args.config == 3 and rank == 0 and world == 1 and args.extras == "all":
         extra = extra_legs(device, peaks)
-    fp8 = fp8_ceiling(device, clocks) if rank == 0 else {}
+    fp8 = fp8_ceiling(device, clocks) if rank == 0 and args.extras == "all" else {}
     clocks.__exit__(None, None, None)
     t_gemm = sum(per[n] for n in path.gemm_names)
     t_dom = sum(per[n] for n in path.dominant)
