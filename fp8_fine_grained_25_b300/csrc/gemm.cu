@@ -17,13 +17,17 @@
 //               sa[m0..m0+127][kb..kb+3] and the tile's sb[nb][kb..kb+3] into a
 //               shared-memory scale ring, so the promotion never waits on a
 //               global load and touches the ring once per 4 K blocks.
+//   warp 3      weight-gradient pair tiles: issues the TMA stores of each
+//               output tile the promotion warps have staged (below).
 //   warps 4-11  promotion + epilogue: tcgen05.ld P_kb (each warp owns 32
 //               TMEM lanes = 32 rows and half of the BN columns), then
 //               acc += P_kb * (sa[m][kb] * sb[n/128][kb]) with packed FP32
 //               FMAs into registers, release the TMEM buffer; after the last
 //               K block convert to bf16 and store (TMA store through a small
 //               swizzled staging buffer for the dense GEMM, masked vector
-//               stores for the grouped one).
+//               stores for the grouped one). Weight-gradient pair tiles stage
+//               the whole tile instead and leave its stores to warp 3, so the
+//               promotion warps start on the next tile at once.
 // Several TMEM buffers let the MMA of later K blocks overlap the promotion
 // of earlier ones. Every wait is bounded in time; on expiry the CTA raises
 // an abort flag, drains its copies and MMAs, frees TMEM and returns.
@@ -72,8 +76,9 @@ constexpr int kScaleKb = 4;     // K blocks of scales per ring slot
 constexpr int kScaleSlots = 4;  // ring slots (16 K blocks staged ahead)
 
 // ROWB: B carries one scale per row (1x128 tiles, the weight-gradient GEMM)
-// instead of one per 128x128 block.
-template <int BN, bool GROUPED, bool PAIR, bool ROWB = false>
+// instead of one per 128x128 block. AEPI: the whole output tile is staged
+// in shared memory and warp 3 issues its TMA stores (pair kernels).
+template <int BN, bool GROUPED, bool PAIR, bool ROWB = false, bool AEPI = false>
 struct Layout {
     static constexpr int A_BYTES = BM * BK;
     // 128-column scale blocks one tile can touch: n0 = BN * t is 128-aligned
@@ -82,12 +87,13 @@ struct Layout {
     static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // rows of B this CTA loads
     static constexpr int B_BYTES = B_ROWS * BK;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    // two 32-row staging boxes per warp, 32 bf16 wide (64-byte swizzle), or
-    // 16 wide (32-byte swizzle) when a warp's columns are not a multiple of
-    // 32: one is filled while the TMA store of the other is still reading
+    // 32-row staging boxes, 32 bf16 wide (64-byte swizzle), or 16 wide
+    // (32-byte swizzle) when a warp's columns are not a multiple of 32. Two
+    // per warp (one is filled while the TMA store of the other is still
+    // reading), or with AEPI all of the warp's 32 x BN/2 outputs.
     static constexpr int EPI_BOX_COLS = (BN / 2) % 32 == 0 ? 32 : 16;
     static constexpr int EPI_BOX_BYTES = 32 * EPI_BOX_COLS * 2;
-    static constexpr int EPI_WARP_BYTES = 2 * EPI_BOX_BYTES;
+    static constexpr int EPI_WARP_BYTES = AEPI ? 32 * (BN / 2) * 2 : 2 * EPI_BOX_BYTES;
     static constexpr int EPI_BYTES = GROUPED ? 0 : kEpiWarps * EPI_WARP_BYTES;
     // slot: sa as [128 rows][kScaleKb], then sb as [MAX_NB][kScaleKb]
     // (ROWB: sb as [kScaleKb][BN], the tile's columns contiguous per K block)
@@ -101,16 +107,19 @@ struct Layout {
                                    (GROUPED ? 4 * (kMaxExperts + 1) : 0);
     static constexpr int STAGES_FIT =
         (kSmemLimit - RESERVE - EPI_BYTES - SCALE_BYTES) / STAGE_BYTES;
-    static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
+    // 256-wide pair tiles measured faster with four stages than with six
+    static constexpr int MAX_STAGES = PAIR && BN == 256 ? 4 : 6;
+    static constexpr int STAGES = STAGES_FIT > MAX_STAGES ? MAX_STAGES : STAGES_FIT;
     static constexpr int EPI_OFF = STAGES * STAGE_BYTES;
     static constexpr int SCALE_OFF = EPI_OFF + EPI_BYTES;
     static constexpr int BAR_OFF = SCALE_OFF + SCALE_BYTES;
     // barriers: full[S], empty[S], tmem_full[NBUF], tmem_empty[NBUF],
-    // scale_full[slots], scale_empty[slots], drain
+    // scale_full[slots], scale_empty[slots], drain, split-K partial and
+    // decided, staged output tile (AEPI) and staging free (AEPI)
     static constexpr int FULL = 0, EMPTY = STAGES, TFULL = 2 * STAGES, TEMPTY = TFULL + NBUF,
                          SFULL = TEMPTY + NBUF, SEMPTY = SFULL + kScaleSlots,
                          DRAIN = SEMPTY + kScaleSlots, PARTIAL = DRAIN + 1, DECIDED = PARTIAL + 1,
-                         NUM_BARS = DECIDED + 1;
+                         EFULL = DECIDED + 1, EFREE = EFULL + 1, NUM_BARS = EFREE + 1;
     static constexpr int MISC_OFF = BAR_OFF + 8 * NUM_BARS;  // tmem slot, abort flag, last-split flag
     static constexpr int TABLE_OFF = MISC_OFF + 16;
     static constexpr int HALF = BN / 2;       // columns per promotion warp
@@ -122,6 +131,7 @@ struct Layout {
                   "stages and their B tiles must start on 1024-byte swizzle atoms");
     static_assert(!(PAIR && GROUPED), "pair mode is for the dense GEMM");
     static_assert(!(ROWB && GROUPED), "row-scaled B is for the dense GEMM");
+    static_assert(!AEPI || (PAIR && ROWB), "the staged-tile epilogue is for weight-gradient pair tiles");
     static_assert(STAGES >= 2, "not enough shared memory for two stages");
     static_assert(8 * NUM_BARS + 16 <= 512, "barrier area overflow");
     static constexpr int smem_bytes(int E) {
@@ -132,6 +142,15 @@ struct Layout {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// First column, within a promotion warp's HALF columns, of its staging box
+// c2 (BC columns wide), which holds acc[BC c2, +BC). When HALF = 16 mod 32
+// the promotion's chunk order puts those at warp columns 16 h + 16 c2, and
+// the last box at HALF - 16 - (HALF - 16) h.
+template <int HALF, int BC>
+__device__ __forceinline__ int epi_box_col(int c2, int h) {
+    return HALF % 32 == 0 ? BC * c2 : c2 < HALF / 16 - 1 ? 16 * h + 16 * c2 : (HALF - 16) * (1 - h);
 }
 
 struct Tile {
@@ -390,7 +409,10 @@ template <int BN, bool GROUPED, bool PAIR, bool ROWB, bool SPLITK>
 __global__ void __launch_bounds__(kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
-    using L = Layout<BN, GROUPED, PAIR, ROWB>;
+    // weight-gradient pair tiles stage the whole output tile and leave its
+    // stores to warp 3; the others keep the two-box epilogue
+    constexpr bool AEPI = PAIR && ROWB && !SPLITK;
+    using L = Layout<BN, GROUPED, PAIR, ROWB, AEPI>;
     constexpr int S = L::STAGES;
     constexpr int NBUF = L::NBUF;
     extern __shared__ uint8_t smem_raw[];
@@ -430,6 +452,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bar(L::DRAIN), 1);
         mbar_init(bar(L::PARTIAL), kEpiWarps);
         mbar_init(bar(L::DECIDED), 1);
+        mbar_init(bar(L::EFULL), kEpiWarps);
+        mbar_init(bar(L::EFREE), 1);
         *abort_flag = 0;
         fence_barrier_init();
         fence_proxy_async_smem();
@@ -646,6 +670,42 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // Let the last copies land before the CTA may exit.
             asm volatile("cp.async.wait_all;" ::: "memory");
+        } else if (warp == 3) {
+            if constexpr (AEPI) {
+                // ------------------------------------------------- C stores
+                // Per tile: wait until the eight promotion warps have staged
+                // their 32 x BN/2 outputs, issue the tile's TMA stores (lane i
+                // those of promotion warp i), and hand the staging back once
+                // the stores have read it. The promotion warps go on to the
+                // next tile meanwhile.
+                uint32_t ephase = 0;
+                bool ok = true;
+                for (int t = unit0; ok && t < num_tiles; t += unit_step) {
+                    const Tile tile = decode_tile<BN, GROUPED, PAIR, SPLITK>(args, table, t, rank);
+                    if (!warp_wait(bar(L::EFULL), ephase, abort_flag, limit)) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane < kEpiWarps) {
+                        constexpr int BC = L::EPI_BOX_COLS;
+                        const int h = lane >> 2;
+                        const int x0 = tile.n0 + h * L::HALF, y = tile.m0 + (lane & 3) * 32;
+                        const uint32_t wbuf = sbase + L::EPI_OFF + lane * L::EPI_WARP_BYTES;
+#pragma unroll 1
+                        for (int c2 = 0; c2 < L::HALF / BC; ++c2) {
+                            const int x = x0 + epi_box_col<L::HALF, BC>(c2, h);
+                            if (x < args.N && y < args.M)
+                                tma_store_2d(&tmC, wbuf + c2 * L::EPI_BOX_BYTES, x, y);
+                        }
+                        bulk_commit_group();
+                        bulk_wait_group_read0();
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(L::EFREE));
+                    ephase ^= 1u;
+                }
+                if (lane < kEpiWarps) bulk_wait_group0();  // writes done before the CTA exits
+            }
         }
     } else {
         // --------------------------------------------- promotion + epilogue
@@ -660,6 +720,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int slot = 0;
         uint32_t sphase = 0;
         uint32_t ebox = 0;  // epilogue boxes staged so far: their buffer alternates
+        uint32_t ephase = 0;  // AEPI: output tiles staged so far (barrier parity)
         uint32_t sred_phase = 0;  // split-K reductions done so far (barrier parity)
         bool ok = true;
         const uint32_t temptry_base = PAIR ? mapa_shared(bar(L::TEMPTY), 0) : bar(L::TEMPTY);
@@ -794,7 +855,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
 
-            if constexpr (!GROUPED) {
+            if constexpr (AEPI) {
+                // bf16 -> the warp's swizzled staging boxes (layout below), all
+                // of them at once, once warp 3 has released the staging (the
+                // previous tile's stores have read it); warp 3 stores them
+                if (!warp_wait(bar(L::EFREE), ephase ^ 1u, abort_flag, limit)) {
+                    ok = false;
+                    break;
+                }
+                constexpr int BC = L::EPI_BOX_COLS;
+                const uint32_t wrow = sbase + L::EPI_OFF + ew * L::EPI_WARP_BYTES + lane * (2 * BC);
+                const uint32_t sw = BC == 32 ? (lane >> 1) & 3 : (lane >> 2) & 1;
+#pragma unroll
+                for (int c2 = 0; c2 < L::HALF / BC; ++c2) {
+#pragma unroll
+                    for (int j = 0; j < BC / 8; ++j) {
+                        const float* v = acc + BC * c2 + 8 * j;
+                        sts_u4(wrow + c2 * L::EPI_BOX_BYTES + ((j ^ sw) << 4), pack_bf16x2(v[0], v[1]),
+                               pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(L::EFULL));
+                ephase ^= 1u;
+            } else if constexpr (!GROUPED) {
                 // bf16 -> swizzled staging (32 rows x EPI_BOX_COLS per box, two
                 // boxes per warp) -> TMA store, one box at a time. Row r of a
                 // box holds EPI_BOX_COLS / 8 16-byte pieces; piece j sits at
@@ -829,10 +914,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
-                    const int wc = L::HALF % 32 == 0 ? BC * c2
-                                   : c2 < L::HALF / 16 - 1 ? 16 * h + 16 * c2
-                                                          : (L::HALF - 16) * (1 - h);
-                    const int x = col0 + wc, y = tile.m0 + quarter * 32;
+                    const int x = col0 + epi_box_col<L::HALF, BC>(c2, h), y = tile.m0 + quarter * 32;
                     if (lane == 0) {
                         if (x < args.N && y < args.M) tma_store_2d(&tmC, ebuf_s, x, y);
                         bulk_commit_group();  // empty when the box lies past C
@@ -890,7 +972,7 @@ cudaError_t prepare(int smem) {
 
 template <int BN, bool GROUPED, bool PAIR, bool ROWB = false, bool SPLITK = false>
 cudaError_t launch_one(const GemmLaunch& g) {
-    using L = Layout<BN, GROUPED, PAIR, ROWB>;
+    using L = Layout<BN, GROUPED, PAIR, ROWB, PAIR && ROWB && !SPLITK>;
     auto kern = fp8_gemm_kernel<BN, GROUPED, PAIR, ROWB, SPLITK>;
     const int smem = L::smem_bytes(GROUPED ? g.args.E : 0);
     cudaError_t err = prepare<BN, GROUPED, PAIR, ROWB, SPLITK>(smem);
@@ -917,7 +999,7 @@ cudaError_t launch_one(const GemmLaunch& g) {
 
 template <int BN, bool ROWB>
 int pair_max_clusters() {
-    using L = Layout<BN, false, true, ROWB>;
+    using L = Layout<BN, false, true, ROWB, ROWB>;
     const int smem = L::smem_bytes(0);
     if (prepare<BN, false, true, ROWB>(smem) != cudaSuccess) return 0;
     cudaLaunchConfig_t cfg = {};
