@@ -412,9 +412,11 @@ int dense_gemm(const void* A, const float* sa, const void* B, const float* sb, v
     if (!make_map_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, K, M, 128, 128) ||
         !make_map_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, K, N, 128, pair ? bn / 2 : bn))
         return FP8Q_ERR_CUDA;
-    const int cbox = fp8q::gemm_c_box_cols(bn);  // 32 (64-byte swizzle) or 16 (32-byte)
+    const int cbox = fp8q::gemm_c_box_cols(bn, pair);  // 64, 32 or 16 columns (128/64/32-byte swizzle)
     if (!make_map_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C_bf16, N, M, cbox, 32,
-                     cbox == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B))
+                     cbox == 64   ? CU_TENSOR_MAP_SWIZZLE_128B
+                     : cbox == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                  : CU_TENSOR_MAP_SWIZZLE_32B))
         return FP8Q_ERR_CUDA;
 
     fp8q::GemmLaunch g{};

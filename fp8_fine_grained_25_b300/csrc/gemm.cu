@@ -87,13 +87,17 @@ struct Layout {
     static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // rows of B this CTA loads
     static constexpr int B_BYTES = B_ROWS * BK;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    // 32-row staging boxes, 32 bf16 wide (64-byte swizzle), or 16 wide
-    // (32-byte swizzle) when a warp's columns are not a multiple of 32. Two
-    // per warp (one is filled while the TMA store of the other is still
-    // reading), or with AEPI all of the warp's 32 x BN/2 outputs.
-    static constexpr int EPI_BOX_COLS = (BN / 2) % 32 == 0 ? 32 : 16;
+    // 32-row staging boxes. Pair tiles stage all of a warp's 32 x BN/2
+    // outputs at once, in boxes 64 bf16 wide (128-byte swizzle), or 16 wide
+    // (32-byte swizzle) when BN/2 is not a multiple of 64, so that a tile
+    // needs one proxy fence and few TMA stores per warp. One-CTA tiles use two
+    // boxes per warp, 32 wide (64-byte swizzle) or 16 wide: one is filled while
+    // the TMA store of the other is still reading.
+    static constexpr bool FULL_STAGE = PAIR && !GROUPED;
+    static constexpr int EPI_BOX_COLS = FULL_STAGE ? ((BN / 2) % 64 == 0 ? 64 : 16)
+                                                   : ((BN / 2) % 32 == 0 ? 32 : 16);
     static constexpr int EPI_BOX_BYTES = 32 * EPI_BOX_COLS * 2;
-    static constexpr int EPI_WARP_BYTES = AEPI ? 32 * (BN / 2) * 2 : 2 * EPI_BOX_BYTES;
+    static constexpr int EPI_WARP_BYTES = FULL_STAGE ? 32 * (BN / 2) * 2 : 2 * EPI_BOX_BYTES;
     static constexpr int EPI_BYTES = GROUPED ? 0 : kEpiWarps * EPI_WARP_BYTES;
     // slot: sa as [128 rows][kScaleKb], then sb as [MAX_NB][kScaleKb]
     // (ROWB: sb as [kScaleKb][BN], the tile's columns contiguous per K block)
@@ -151,6 +155,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 template <int HALF, int BC>
 __device__ __forceinline__ int epi_box_col(int c2, int h) {
     return HALF % 32 == 0 ? BC * c2 : c2 < HALF / 16 - 1 ? 16 * h + 16 * c2 : (HALF - 16) * (1 - h);
+}
+
+// Row r of a BC-column staging box holds BC / 8 16-byte pieces; the TMA
+// swizzle puts piece j at j ^ (r % 8) (128-byte swizzle, 64 columns),
+// j ^ (r / 2 % 4) (64-byte, 32 columns) or j ^ (r / 4 % 2) (32-byte, 16).
+template <int BC>
+__device__ __forceinline__ uint32_t epi_swizzle(int r) {
+    return BC == 64 ? r & 7 : BC == 32 ? (r >> 1) & 3 : (r >> 2) & 1;
 }
 
 struct Tile {
@@ -865,7 +877,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 constexpr int BC = L::EPI_BOX_COLS;
                 const uint32_t wrow = sbase + L::EPI_OFF + ew * L::EPI_WARP_BYTES + lane * (2 * BC);
-                const uint32_t sw = BC == 32 ? (lane >> 1) & 3 : (lane >> 2) & 1;
+                const uint32_t sw = epi_swizzle<BC>(lane);
 #pragma unroll
                 for (int c2 = 0; c2 < L::HALF / BC; ++c2) {
 #pragma unroll
@@ -879,15 +891,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(L::EFULL));
                 ephase ^= 1u;
+            } else if constexpr (L::FULL_STAGE) {
+                // bf16 -> all of the warp's swizzled staging boxes (box c2
+                // holds acc[BC c2, +BC), see epi_box_col), one proxy fence, then
+                // the boxes' TMA stores. The previous tile's stores finished
+                // reading the staging long ago; wait for that all the same.
+                constexpr int BC = L::EPI_BOX_COLS;
+                if (lane == 0) bulk_wait_group_read0();
+                __syncwarp();
+                const uint32_t wrow = sbase + L::EPI_OFF + ew * L::EPI_WARP_BYTES + lane * (2 * BC);
+                const uint32_t sw = epi_swizzle<BC>(lane);
+#pragma unroll
+                for (int c2 = 0; c2 < L::HALF / BC; ++c2) {
+#pragma unroll
+                    for (int j = 0; j < BC / 8; ++j) {
+                        const float* v = acc + BC * c2 + 8 * j;
+                        sts_u4(wrow + c2 * L::EPI_BOX_BYTES + ((j ^ sw) << 4), pack_bf16x2(v[0], v[1]),
+                               pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    const uint32_t wbuf = sbase + L::EPI_OFF + ew * L::EPI_WARP_BYTES;
+                    const int y = tile.m0 + quarter * 32;
+#pragma unroll
+                    for (int c2 = 0; c2 < L::HALF / BC; ++c2) {
+                        const int x = col0 + epi_box_col<L::HALF, BC>(c2, h);
+                        if (x < args.N && y < args.M) tma_store_2d(&tmC, wbuf + c2 * L::EPI_BOX_BYTES, x, y);
+                    }
+                    bulk_commit_group();
+                }
             } else if constexpr (!GROUPED) {
                 // bf16 -> swizzled staging (32 rows x EPI_BOX_COLS per box, two
-                // boxes per warp) -> TMA store, one box at a time. Row r of a
-                // box holds EPI_BOX_COLS / 8 16-byte pieces; piece j sits at
-                // j ^ (r / 2 % 4) for the 64-byte swizzle (32 columns) and at
-                // j ^ (r / 4 % 2) for the 32-byte swizzle (16 columns). Box c2
-                // stores acc[BC c2, +BC); when HALF = 16 mod 32 those are warp
-                // columns 16 h + 16 c2, and HALF - 16 - (HALF - 16) h for the
-                // last box (the promotion's chunk order).
+                // boxes per warp, pieces placed by epi_swizzle) -> TMA store, one
+                // box at a time. Box c2 stores acc[BC c2, +BC) (see epi_box_col).
                 constexpr int BC = L::EPI_BOX_COLS;
                 uint8_t* ebuf0 = smem + L::EPI_OFF + ew * L::EPI_WARP_BYTES;
                 const uint32_t ebuf0_s = sbase + L::EPI_OFF + ew * L::EPI_WARP_BYTES;
@@ -909,7 +947,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         pk.y = pack_bf16x2(v[2], v[3]);
                         pk.z = pack_bf16x2(v[4], v[5]);
                         pk.w = pack_bf16x2(v[6], v[7]);
-                        const int phys = BC == 32 ? j ^ ((lane >> 1) & 3) : j ^ ((lane >> 2) & 1);
+                        const int phys = j ^ static_cast<int>(epi_swizzle<BC>(lane));
                         *reinterpret_cast<uint4*>(ebuf + lane * (2 * BC) + phys * 16) = pk;
                     }
                     fence_proxy_async_smem();
@@ -1030,11 +1068,11 @@ int gemm_stages(int bn) {
     }
 }
 
-int gemm_c_box_cols(int bn) {
+int gemm_c_box_cols(int bn, bool pair) {
     switch (bn) {
-        case 128: return Layout<128, false, false>::EPI_BOX_COLS;
-        case 224: return Layout<224, false, false>::EPI_BOX_COLS;
-        case 256: return Layout<256, false, false>::EPI_BOX_COLS;
+        case 128: return pair ? Layout<128, false, true>::EPI_BOX_COLS : Layout<128, false, false>::EPI_BOX_COLS;
+        case 224: return pair ? Layout<224, false, true>::EPI_BOX_COLS : Layout<224, false, false>::EPI_BOX_COLS;
+        case 256: return pair ? Layout<256, false, true>::EPI_BOX_COLS : Layout<256, false, false>::EPI_BOX_COLS;
         default: return 0;
     }
 }

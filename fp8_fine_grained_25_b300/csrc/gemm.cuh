@@ -50,8 +50,9 @@ struct GemmLaunch {
 cudaError_t launch_gemm(const GemmLaunch& g);
 int gemm_stages(int bn);
 // Columns of the TMA-store box of C the kernel writes through (the tensor
-// map's box width; 32 with a 64-byte swizzle, or 16 with a 32-byte swizzle).
-int gemm_c_box_cols(int bn);
+// map's box width: 64 with a 128-byte swizzle, 32 with a 64-byte swizzle, or
+// 16 with a 32-byte swizzle), for one-CTA or pair tiles.
+int gemm_c_box_cols(int bn, bool pair);
 // Pair mode: how many 2-CTA clusters of the dense kernel fit on the device
 // at once (0 if none or on error).
 int gemm_pair_max_clusters(int bn, bool row_scaled_b);
