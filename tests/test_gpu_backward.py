@@ -156,6 +156,24 @@ def test_wgrad_gemm_random_codes_full_output(q, M, N, K, bn, pairs):
     assert q.fp8q_get_device_status() == 0
 
 
+@pytest.mark.parametrize("bn", [128, 256])
+def test_wgrad_gemm_several_tiles_per_cluster(q, bn):
+    """4096 x 2056 outputs in 256-row pair tiles are 2-4 tiles per 2-CTA
+    cluster: warp 3 stores each staged tile while the promotion warps go on
+    to the next one, and the staging is reused only after those stores have
+    read it (ragged last n-tile included); full output, two runs in a row."""
+    qa, sa, qb, sb = _rowscaled_operands(4096, 2056, 256, 19 + bn)
+    c32, S = oracle.wgrad_gemm(qa, sa, qb, sb)
+    q.fp8q_set_gemm_tile_n(bn)
+    try:
+        for rep in range(2):
+            C = _run_wgrad(q, qa, sa, qb, sb)
+            assert q.fp8q_get_device_status() == 0
+            assert_gemm_ok(to_f32(C), c32, S, f"wgrad 4096x2056x256 bn={bn} run {rep}")
+    finally:
+        q.fp8q_set_gemm_tile_n(0)
+
+
 def test_wgrad_gemm_uses_each_b_row_scale(q):
     # B scales that differ by row inside one 128-row block: a kernel that
     # took one scale per block would be off by the ratio.

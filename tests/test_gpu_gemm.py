@@ -101,6 +101,24 @@ def test_gemm_tile_widths_agree_bitwise(q, pairs):
         assert torch.equal(out[bn].view(torch.int16), out[256].view(torch.int16)), bn
 
 
+@pytest.mark.parametrize("bn", [128, 224, 256])
+def test_gemm_several_tiles_per_cluster(q, bn):
+    """4096 x 2048 outputs in 256-row pair tiles are 2-4 tiles per 2-CTA
+    cluster, so each CTA stages and stores several output tiles through the
+    same shared memory (224 wide: a 32-column last tile); the full output is
+    checked on two runs in a row."""
+    qa, sa, qb, sb = _random_operands(4096, 2048, 256, 11 + bn)
+    c32, S = oracle.gemm(qa, sa, qb, sb)
+    q.fp8q_set_gemm_tile_n(bn)
+    try:
+        for rep in range(2):
+            C = _run(q, qa, sa, qb, sb)
+            assert q.fp8q_get_device_status() == 0
+            assert_gemm_ok(to_f32(C), c32, S, f"gemm 4096x2048x256 bn={bn} run {rep}")
+    finally:
+        q.fp8q_set_gemm_tile_n(0)
+
+
 def test_gemm_repeatable(q):
     qa, sa, qb, sb = _random_operands(256, 512, 768, 9)
     c1 = _run(q, qa, sa, qb, sb).clone()
