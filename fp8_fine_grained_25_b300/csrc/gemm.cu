@@ -23,11 +23,13 @@
 //               TMEM lanes = 32 rows and half of the BN columns), then
 //               acc += P_kb * (sa[m][kb] * sb[n/128][kb]) with packed FP32
 //               FMAs into registers, release the TMEM buffer; after the last
-//               K block convert to bf16 and store (TMA store through a small
-//               swizzled staging buffer for the dense GEMM, masked vector
-//               stores for the grouped one). Weight-gradient pair tiles stage
-//               the whole tile instead and leave its stores to warp 3, so the
-//               promotion warps start on the next tile at once.
+//               K block convert to bf16 and store: TMA stores through
+//               swizzled shared-memory staging for the dense GEMM (pair tiles
+//               stage a warp's whole slice at once, one-CTA tiles two boxes
+//               at a time), masked vector stores for the grouped one.
+//               Weight-gradient pair tiles leave the stores of the staged
+//               tile to warp 3, so the promotion warps start on the next
+//               tile at once.
 // Several TMEM buffers let the MMA of later K blocks overlap the promotion
 // of earlier ones. Every wait is bounded in time; on expiry the CTA raises
 // an abort flag, drains its copies and MMAs, frees TMEM and returns.
