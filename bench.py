@@ -830,7 +830,7 @@ def extra_legs(device, peaks):
         "hbm_frac": (wbytes + abytes) / t / 1e9 / peaks["hbm_gbs"],
         "roofline_ms": roof_t * 1e3, "frac_of_roofline": roof_t / t,
         "bytes_per_launch": wbytes + abytes, "flops_per_launch": fl,
-        "traffic_bytes_per_launch": profiled_traffic("gemm_grouped_moe.md", "gemm.cu"),
+        "traffic_bytes_per_launch": profiled_traffic("gemm_grouped_moe.md", "gemm_kernel.cuh"),
         "timed": "alone, back to back, mean of the middle 12 of 20 (weights 3.76 GB > L2)"}
     del qa, sa, qw, sw, C, w
     torch.cuda.empty_cache()
@@ -942,17 +942,17 @@ def main():
     traffic = None
     kernel_profiles = {}
     if args.config == 3:
-        traffic = profiled_traffic("gemm_dense_8192x7168x7168.md", "gemm.cu")
+        traffic = profiled_traffic("gemm_dense_8192x7168x7168.md", "gemm_kernel.cuh")
         kernel_profiles = {"quant_act": ("quant_act_8192x7168.md", "quant.cu"),
                            "quant_weight[B]": ("quant_weight_7168x7168.md", "quant.cu")}
     elif args.config == 9:
         traffic = profiled_traffic("gemm_ue8m0_dense_8192x7168x7168.md", "gemm_bs.cu")
         kernel_profiles = {"quant_act": ("quant_ue8m0_8192x7168.md", "quant.cu")}
     elif args.config == 8:
-        traffic = profiled_traffic("gemm_wgrad_7168x7168x8192.md", "gemm.cu")
+        traffic = profiled_traffic("gemm_wgrad_7168x7168x8192.md", "gemm_kernel.cuh")
         kernel_profiles = {"quant_act[dY]": ("quant_act_8192x7168.md", "quant.cu"),
                            "quant_weight_t[W]": ("quant_weight_t_7168x7168.md", "quant.cu"),
-                           "gemm[dX]": ("gemm_dense_8192x7168x7168.md", "gemm.cu"),
+                           "gemm[dX]": ("gemm_dense_8192x7168x7168.md", "gemm_kernel.cuh"),
                            "quant_act_t[dY]": ("quant_act_t_8192x7168.md", "quant.cu"),
                            "quant_act_t[X]": ("quant_act_t_8192x7168.md", "quant.cu")}
     for kname, (prof, src_file) in kernel_profiles.items():

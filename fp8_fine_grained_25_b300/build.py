@@ -18,8 +18,11 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libfp8q.so")
-SOURCES = ["api.cu", "quant.cu", "gemm.cu", "gemm_bs.cu"]
-HEADERS = ["ptx.cuh", "gemm.cuh", "quant.cuh"]
+SOURCES = ["api.cu", "quant.cu", "gemm.cu", "gemm_pair.cu", "gemm_bs.cu"]
+HEADERS = ["ptx.cuh", "gemm.cuh", "gemm_kernel.cuh", "quant.cuh"]
+# ptxas options per source: the block-scaled dense GEMM's pair-tile kernels
+# measured faster at -O1 (see gemm_pair.cu); everything else uses the default
+PTXAS = {"gemm_pair.cu": ["-Xptxas", "-O1"]}
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -48,15 +51,28 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if not force and up_to_date():
         return LIB
     tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared", "-Xcompiler", "-fPIC,-fvisibility=hidden",
-           "-I", INCLUDE, "-I", CSRC, "-o", tmp, *[os.path.join(CSRC, s) for s in SOURCES]]
-    if verbose:
-        cmd.insert(1, "-Xptxas=-v")
-    res = subprocess.run(cmd, capture_output=True, text=True)
-    if res.returncode != 0:
-        raise RuntimeError("nvcc failed:\n" + res.stdout + res.stderr)
-    if verbose:
-        sys.stderr.write(res.stdout + res.stderr)
+    common = [*ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",
+              "-I", INCLUDE, "-I", CSRC]
+    objs = []
+    try:
+        for src in SOURCES:
+            obj = f"{tmp}.{src}.o"
+            cmd = [nvcc(), *common, *PTXAS.get(src, []), "-c", os.path.join(CSRC, src), "-o", obj]
+            if verbose:
+                cmd.insert(1, "-Xptxas=-v")
+            res = subprocess.run(cmd, capture_output=True, text=True)
+            if res.returncode != 0:
+                raise RuntimeError(f"nvcc failed on {src}:\n" + res.stdout + res.stderr)
+            if verbose:
+                sys.stderr.write(res.stdout + res.stderr)
+            objs.append(obj)
+        res = subprocess.run([nvcc(), *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
+        if res.returncode != 0:
+            raise RuntimeError("nvcc link failed:\n" + res.stdout + res.stderr)
+    finally:
+        for obj in objs:
+            if os.path.exists(obj):
+                os.remove(obj)
     os.replace(tmp, LIB)
     return LIB
 

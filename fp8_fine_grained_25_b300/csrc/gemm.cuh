@@ -58,6 +58,13 @@ int gemm_c_box_cols(int bn, bool pair);
 int gemm_pair_max_clusters(int bn, bool row_scaled_b);
 cudaError_t read_device_status(cudaStream_t stream, uint32_t* out, bool clear);
 
+// gemm_pair.cu: the pair tiles of the block-scaled dense GEMM (launch, the
+// co-resident cluster count, and that unit's device status word, read after
+// the caller's stream synchronisation).
+cudaError_t launch_gemm_dense_pair(const GemmLaunch& g);
+int gemm_dense_pair_max_clusters(int bn);
+cudaError_t read_dense_pair_status(uint32_t* out, bool clear);
+
 // The GEMM with UE8M0 block scales applied by the tensor core (gemm_bs.cu):
 // output tiles of 128 x gemm_bs_tile_n() per CTA; tmB's box is that many
 // rows, or half of them in pair mode (2-CTA clusters, 256-row tiles).
