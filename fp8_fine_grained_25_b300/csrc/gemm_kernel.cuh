@@ -428,6 +428,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // pair tiles stage the whole output tile and leave its stores to warp 3
     // (split K keeps the promotion warps' own stores)
     constexpr bool AEPI = PAIR && !GROUPED && !SPLITK;
+    // ... except a CTA's last tile, which has nothing to overlap its stores
+    // with: the narrower pair tiles (one wave at the MLA shapes) store it
+    // from the promotion warps; 256-wide tiles measured faster without the
+    // extra branch
+    constexpr bool LAST_DIRECT = AEPI && BN != 256;
     using L = Layout<BN, GROUPED, PAIR, ROWB, AEPI>;
     constexpr int S = L::STAGES;
     constexpr int NBUF = L::NBUF;
@@ -697,6 +702,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t ephase = 0;
                 bool ok = true;
                 for (int t = unit0; ok && t < num_tiles; t += unit_step) {
+                    if (LAST_DIRECT && t + unit_step >= num_tiles) break;
                     const Tile tile = decode_tile<BN, GROUPED, PAIR, SPLITK>(args, table, t, rank);
                     if (!warp_wait(bar(L::EFULL), ephase, abort_flag, limit)) {
                         ok = false;
@@ -893,7 +899,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(L::EFULL));
+                if (!LAST_DIRECT || t + unit_step < num_tiles) {
+                    if (lane == 0) mbar_arrive(bar(L::EFULL));
+                } else if (lane == 0) {
+                    const uint32_t wbuf = sbase + L::EPI_OFF + ew * L::EPI_WARP_BYTES;
+                    const int y = tile.m0 + quarter * 32;
+#pragma unroll
+                    for (int c2 = 0; c2 < L::HALF / BC; ++c2) {
+                        const int x = col0 + epi_box_col<L::HALF, BC>(c2, h);
+                        if (x < args.N && y < args.M) tma_store_2d(&tmC, wbuf + c2 * L::EPI_BOX_BYTES, x, y);
+                    }
+                    bulk_commit_group();
+                }
                 ephase ^= 1u;
             } else if constexpr (L::FULL_STAGE) {
                 // bf16 -> all of the warp's swizzled staging boxes (box c2
