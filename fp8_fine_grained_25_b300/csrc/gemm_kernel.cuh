@@ -17,8 +17,8 @@
 //               sa[m0..m0+127][kb..kb+3] and the tile's sb[nb][kb..kb+3] into a
 //               shared-memory scale ring, so the promotion never waits on a
 //               global load and touches the ring once per 4 K blocks.
-//   warp 3      weight-gradient pair tiles: issues the TMA stores of each
-//               output tile the promotion warps have staged (below).
+//   warp 3      pair tiles: issues the TMA stores of each output tile the
+//               promotion warps have staged (below).
 //   warps 4-11  promotion + epilogue: tcgen05.ld P_kb (each warp owns 32
 //               TMEM lanes = 32 rows and half of the BN columns), then
 //               acc += P_kb * (sa[m][kb] * sb[n/128][kb]) with packed FP32
@@ -27,9 +27,9 @@
 //               swizzled shared-memory staging for the dense GEMM (pair tiles
 //               stage a warp's whole slice at once, one-CTA tiles two boxes
 //               at a time), masked vector stores for the grouped one.
-//               Weight-gradient pair tiles leave the stores of the staged
-//               tile to warp 3, so the promotion warps start on the next
-//               tile at once.
+//               Pair tiles leave the stores of the staged tile to warp 3
+//               (but for a CTA's last 128- or 224-wide tile), so the
+//               promotion warps start on the next tile at once.
 // Several TMEM buffers let the MMA of later K blocks overlap the promotion
 // of earlier ones. Every wait is bounded in time; on expiry the CTA raises
 // an abort flag, drains its copies and MMAs, frees TMEM and returns.
@@ -500,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int KB = args.KB;
 
     // Registers: 384 threads launch with 168 each (64512). The control
-    // warpgroup (producer, MMA, scale loader, one idle warp) gives most of its
+    // warpgroup (producer, MMA, scale loader, store warp) gives most of its
     // share to the two promotion warpgroups, which hold a 128 x BN/2 FP32
     // accumulator slice (BN/2 registers per thread) plus two 32-column TMEM
     // chunks: 128 * 40 + 256 * 232 = 64512.
