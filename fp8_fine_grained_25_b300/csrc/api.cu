@@ -25,9 +25,9 @@ struct DeviceInfo {
     bool supported = false;
     int sms = 0;
     // co-resident 2-CTA clusters of the pair kernel, per tile width
-    // ([0]: 128, [1]: 256, [2]: 224) and B-scale layout ([0]: 128x128 blocks,
-    // [1]: one per row); -1: not queried yet
-    int pair_clusters[3][2] = {{-1, -1}, {-1, -1}, {-1, -1}};
+    // ([0]: 128, [1]: 256, [2]: 224, [3]: 160) and B-scale layout ([0]:
+    // 128x128 blocks, [1]: one per row); -1: not queried yet
+    int pair_clusters[4][2] = {{-1, -1}, {-1, -1}, {-1, -1}, {-1, -1}};
     int bs_pair_clusters[2] = {-1, -1};  // the same for the UE8M0 (hardware-scaled) GEMM
 };
 
@@ -98,20 +98,36 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Output-tile width by a wave model: waves of tiles over the SMs times the
-// tile's cost, its width plus a fixed share for the per-K-block handshake
-// that does not shrink with the width. The shares reproduce measured
-// per-column costs relative to 256: 1.2 for 128 and ~1.08 for 224 (in long
-// power-capped runs). 224 (block-scaled B only) wins where it saves a wave
-// or wasted columns (2048 x 7168, N = 576); at 8192 x 7168 its 6 % wave
-// saving does not pay, and 256 stays. Ties keep the earlier candidate.
-int choose_bn(int64_t M, int64_t N, int sms, bool allow224) {
+// Output-tile width by a wave model: rounds of work units over the units
+// that run at once, times the cost of one unit at that width.
+// Pair tiles of the block-scaled GEMM (256 rows on a 2-CTA cluster, 74
+// clusters): a unit's cost relative to 256 columns, measured back to back
+// at 2032 MHz on 4096 x {576, 1536}, 2048 x 7168 and 8192 x {2048, 7168}
+// (K = 7168): 0.74 for 128, 0.85 for 160, 0.97 for 224. The K loop costs
+// ~600-740 cycles per K block at every width, so narrow tiles pay only
+// where they save a round: 160 at 4096 x 576 (one round of 64 units instead
+// of two of 80 at 128; 24.8 against 26.9 us at 224), 224 at 4096 x 1536
+// and 2048 x 7168, 256 for the large layers.
+// One-CTA tiles and the row-scaled GEMM: tiles over the SMs, a tile costing
+// its width plus a fixed share for the per-K-block handshake; the shares
+// reproduce measured per-column costs relative to 256 of 1.2 for 128 and
+// ~1.08 for 224 (in long power-capped runs).
+// Ties keep the earlier candidate.
+int choose_bn(int64_t M, int64_t N, int sms, bool block_scaled, bool pair) {
     int best = 256;
     int64_t best_cost = -1;
-    for (int bn : {256, 128, 224}) {
-        if (bn == 224 && !allow224) continue;
-        const int64_t tiles = cdiv(M, 128) * cdiv(N, bn);
-        const int64_t cost = cdiv(tiles, sms) * (bn + (bn == 224 ? 80 : 64));
+    for (int bn : {256, 128, 224, 160}) {
+        if ((bn == 224 || bn == 160) && !block_scaled) continue;
+        if (bn == 160 && !pair) continue;
+        int64_t cost;
+        if (pair && block_scaled) {
+            const int64_t units = cdiv(cdiv(M, 128), 2) * cdiv(N, bn);
+            const int unit_cost = bn == 128 ? 237 : bn == 160 ? 272 : bn == 224 ? 310 : 320;
+            cost = cdiv(units, std::max(1, sms / 2)) * unit_cost;
+        } else {
+            const int64_t tiles = cdiv(M, 128) * cdiv(N, bn);
+            cost = cdiv(tiles, sms) * (bn + (bn == 224 ? 80 : 64));
+        }
         if (best_cost < 0 || cost < best_cost) {
             best = bn;
             best_cost = cost;
@@ -168,7 +184,7 @@ const char* fp8q_status_string(int status) {
 void fp8q_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns = ns ? ns : 1000000000ull; }
 
 int fp8q_set_gemm_tile_n(int bn) {
-    if (bn != 0 && bn != 128 && bn != 224 && bn != 256) return FP8Q_ERR_UNSUPPORTED;
+    if (bn != 0 && bn != 128 && bn != 160 && bn != 224 && bn != 256) return FP8Q_ERR_UNSUPPORTED;
     g_force_bn = bn;
     return FP8Q_OK;
 }
@@ -359,27 +375,45 @@ struct DensePlan {
     int64_t slots; // units that run at once
 };
 
+// Co-resident clusters of the pair kernel of tile width bn (queried once).
+int pair_clusters(DeviceInfo* dev, int bn, bool row_scaled_b) {
+    int* pc = &dev->pair_clusters[bn == 256 ? 1 : bn == 224 ? 2 : bn == 160 ? 3 : 0][row_scaled_b ? 1 : 0];
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (*pc < 0) *pc = fp8q::gemm_pair_max_clusters(bn, row_scaled_b);
+    return *pc;
+}
+
 int plan_dense(DeviceInfo* dev, int64_t M, int64_t N, bool row_scaled_b, DensePlan* p) {
-    // the 224-wide tile exists for block-scaled B only; a forced 224 runs the
-    // row-scaled GEMM 256 wide
-    int bn = g_force_bn ? g_force_bn : choose_bn(M, N, dev->sms, !row_scaled_b);
-    if (bn == 224 && row_scaled_b) bn = 256;
     // 2-CTA pairs (256-row tiles over two SMs) when there are at least two
     // m-tiles to pair.
-    bool pair = g_pair_mode && M > 128;
-    int* pc = &dev->pair_clusters[bn == 256 ? 1 : bn == 224 ? 2 : 0][row_scaled_b ? 1 : 0];
-    if (pair) {
-        std::lock_guard<std::mutex> lock(g_mutex);
-        if (*pc < 0) *pc = fp8q::gemm_pair_max_clusters(bn, row_scaled_b);
-        pair = *pc > 0;
+    const bool want_pair = g_pair_mode && M > 128;
+    // the 160- and 224-wide tiles exist for block-scaled B only; forced,
+    // they run the row-scaled GEMM 256 wide
+    int bn = g_force_bn ? g_force_bn : choose_bn(M, N, dev->sms, !row_scaled_b, want_pair);
+    if ((bn == 224 || bn == 160) && row_scaled_b) bn = 256;
+    int clusters = want_pair ? pair_clusters(dev, bn, row_scaled_b) : 0;
+    bool pair = clusters > 0;
+    if (bn == 160 && !pair) {
+        // 160-wide tiles are pair tiles only: the best one-CTA width
+        bn = choose_bn(M, N, dev->sms, !row_scaled_b, false);
+        clusters = 0;
     }
     p->bn = bn;
     p->pair = pair;
-    p->clusters = pair ? *pc : 0;
+    p->clusters = clusters;
     const int64_t mt = cdiv(M, 128);
     p->units = (pair ? cdiv(mt, 2) : mt) * cdiv(N, bn);
-    p->slots = pair ? *pc : dev->sms;
+    p->slots = pair ? clusters : dev->sms;
     return FP8Q_OK;
+}
+
+// K ranges of a split-K call with this plan before the workspace limit: the
+// forced or chosen count, at most one range per 4 K blocks; 1 for 160-wide
+// tiles, which have no split-K form.
+int plan_splits(const DensePlan& plan, int64_t K) {
+    if (plan.bn == 160) return 1;
+    const int splits = g_force_splits ? g_force_splits : choose_splits(plan.units, plan.slots, cdiv(K, 128));
+    return static_cast<int>(std::min<int64_t>(splits, cdiv(cdiv(K, 128), 4)));
 }
 
 int dense_gemm(const void* A, const float* sa, const void* B, const float* sb, void* C_bf16,
@@ -403,9 +437,7 @@ int dense_gemm(const void* A, const float* sa, const void* B, const float* sb, v
     // count, reduced until the workspace holds it
     int splits = 1;
     if (workspace && !row_scaled_b) {
-        splits = g_force_splits ? g_force_splits
-                                : choose_splits(plan.units, plan.slots, cdiv(K, 128));
-        splits = static_cast<int>(std::min<int64_t>(splits, cdiv(cdiv(K, 128), 4)));
+        splits = plan_splits(plan, K);
         while (splits > 1 && splitk_bytes(M, N, splits, bn) > workspace_bytes) --splits;
     }
     CUtensorMap tmA, tmB, tmC;
@@ -484,9 +516,7 @@ int fp8_block_gemm_workspace_size(int64_t M, int64_t N, int64_t K, size_t* bytes
     if (int rc = current_device(&dev)) return rc;
     DensePlan plan;
     plan_dense(dev, M, N, false, &plan);
-    int splits = g_force_splits ? g_force_splits : choose_splits(plan.units, plan.slots, cdiv(K, 128));
-    splits = static_cast<int>(std::min<int64_t>(splits, cdiv(cdiv(K, 128), 4)));
-    *bytes = splitk_bytes(M, N, splits, plan.bn);
+    *bytes = splitk_bytes(M, N, plan_splits(plan, K), plan.bn);
     return FP8Q_OK;
 }
 
@@ -644,9 +674,7 @@ int fp8_block_gemm_static(const void* A, const float* sa, const void* B, const f
     // the split count this call runs with, and the scratch it needs
     DensePlan plan;
     plan_dense(dev, M, N, false, &plan);
-    int splits = g_force_splits ? g_force_splits : choose_splits(plan.units, plan.slots, cdiv(K, 128));
-    splits = static_cast<int>(std::min<int64_t>(splits, cdiv(cdiv(K, 128), 4)));
-    const size_t need = splitk_bytes(M, N, splits, plan.bn);
+    const size_t need = splitk_bytes(M, N, plan_splits(plan, K), plan.bn);
     if (need > FP8Q_STATIC_SCRATCH_BYTES) return FP8Q_ERR_SHAPE;
     if (need == 0) return dense_gemm(A, sa, B, sb, C_bf16, M, N, K, false, nullptr, 0, stream);
     int d = 0;

@@ -18,6 +18,7 @@ int gemm_stages(int bn) {
 int gemm_c_box_cols(int bn, bool pair) {
     switch (bn) {
         case 128: return pair ? Layout<128, false, true>::EPI_BOX_COLS : Layout<128, false, false>::EPI_BOX_COLS;
+        case 160: return pair ? Layout<160, false, true>::EPI_BOX_COLS : 0;  // pair tiles only
         case 224: return pair ? Layout<224, false, true>::EPI_BOX_COLS : Layout<224, false, false>::EPI_BOX_COLS;
         case 256: return pair ? Layout<256, false, true>::EPI_BOX_COLS : Layout<256, false, false>::EPI_BOX_COLS;
         default: return 0;

@@ -39,7 +39,7 @@ struct GemmLaunch {
     const CUtensorMap* tmB;
     const CUtensorMap* tmC;
     GemmArgs args;
-    int bn;                  // 128, 224 (dense, block-scaled B) or 256
+    int bn;                  // 128, 160 (pair tiles), 224 (both: dense, block-scaled B) or 256
     bool grouped;
     bool pair;               // 2-CTA clusters with the 2-CTA MMA (dense only)
     bool row_scaled_b;       // sb holds one scale per row of B (dense only)

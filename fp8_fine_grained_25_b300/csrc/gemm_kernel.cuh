@@ -4,8 +4,8 @@
 // "FP8 低精度训练": "细粒度量化" Fig. 7a for the scale granularity,
 // "提高累加精度" Fig. 7b for the promotion into FP32 registers).
 //
-// Per CTA (persistent, one 128 x BN output tile at a time, BN = 128, 224 or
-// 256, 12 warps):
+// Per CTA (persistent, one 128 x BN output tile at a time, BN = 128, 160,
+// 224 or 256, 12 warps):
 //   warp 0      TMA producer: per K block, a 128x128 A box and a BNx128 B box
 //               (E4M3, 128-byte swizzle) into a ring of shared-memory stages.
 //   warp 1      MMA issuer: 4 x tcgen05.mma kind::f8f6f4 (K = 32 each) write
@@ -28,7 +28,7 @@
 //               stage a warp's whole slice at once, one-CTA tiles two boxes
 //               at a time), masked vector stores for the grouped one.
 //               Pair tiles leave the stores of the staged tile to warp 3
-//               (but for a CTA's last 128- or 224-wide tile), so the
+//               (but for a CTA's last tile narrower than 256), so the
 //               promotion warps start on the next tile at once.
 // Several TMEM buffers let the MMA of later K blocks overlap the promotion
 // of earlier ones. Every wait is bounded in time; on expiry the CTA raises
@@ -39,7 +39,10 @@
 // multiple of 32 but not of 128: the scale ring carries up to three
 // 128-column B-scale blocks, each promotion warp's 112 columns touch at most
 // two (two scale products per K block), and the warp reads TMEM in 32-column
-// chunks that start on multiples of 32 plus one 16-column chunk.
+// chunks that start on multiples of 32 plus one 16-column chunk. Tile width
+// 160 (pair tiles of the block-scaled dense GEMM only) works the same way
+// with 80 columns per warp; three of its accumulators fit in TMEM, so the
+// MMA can run two K blocks ahead of the promotion instead of one.
 //
 // Pair mode (dense GEMM): two CTAs of a cluster compute a 256 x BN tile with
 // the 2-CTA MMA (tcgen05 cta_group::2). Each CTA holds its own 128 rows of A
@@ -86,7 +89,7 @@ template <int BN, bool GROUPED, bool PAIR, bool ROWB = false, bool AEPI = false>
 struct Layout {
     static constexpr int A_BYTES = BM * BK;
     // 128-column scale blocks one tile can touch: n0 = BN * t is 128-aligned
-    // for BN = 128 and 256; a 224-wide tile can start inside a block
+    // for BN = 128 and 256; a 160- or 224-wide tile can start inside a block
     static constexpr int MAX_NB = BN % 128 == 0 ? BN / 128 : BN / 128 + 2;
     static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // rows of B this CTA loads
     static constexpr int B_BYTES = B_ROWS * BK;
@@ -132,8 +135,9 @@ struct Layout {
     static constexpr int TABLE_OFF = MISC_OFF + 16;
     static constexpr int HALF = BN / 2;       // columns per promotion warp
     static constexpr int CHUNKS = HALF / 32;  // 32-column TMEM loads, issued in pairs
-    static_assert(BN == 128 || BN == 224 || BN == 256, "tile width must be 128, 224 or 256");
-    static_assert(HALF % 32 == 0 || (!GROUPED && !ROWB), "224-wide tiles are for the block-scaled dense GEMM");
+    static_assert(BN == 128 || BN == 160 || BN == 224 || BN == 256, "tile width must be 128, 160, 224 or 256");
+    static_assert(BN != 160 || (PAIR && !GROUPED && !ROWB), "160-wide tiles are pair tiles of the block-scaled dense GEMM");
+    static_assert(HALF % 32 == 0 || (!GROUPED && !ROWB), "160- and 224-wide tiles are for the block-scaled dense GEMM");
     static_assert(HALF % 32 == 16 || CHUNKS % 2 == 0, "32-column TMEM chunks are loaded in pairs");
     static_assert((B_ROWS * BK) % 1024 == 0 && STAGE_BYTES % 1024 == 0,
                   "stages and their B tiles must start on 1024-byte swizzle atoms");
@@ -286,35 +290,49 @@ __device__ __forceinline__ void fma_cols(float (&acc)[HALF], const uint32_t* r, 
 }
 
 // Promotion of one warp's HALF columns when HALF = 16 mod 32 (112 of a
-// 224-wide tile), the same code for both warpgroups (h):
+// 224-wide tile, 80 of a 160-wide one), the same code for both warpgroups (h):
 // 32-column chunks at warp columns b + 32 i (b = 16 h) into acc[32 i, +32),
 // i < HALF / 32, and a 16-column chunk at column (HALF - 16) (1 - h) into
 // acc[HALF - 16, HALF). Every 32-column chunk then starts on a multiple of 32
 // (the tile starts on one; a warpgroup's HALF columns leave 16 over), so
 // none crosses a 128-column scale block: a chunk at warp column o uses cs
-// when o < split, else csn. Two TMEM loads per wait.
+// when o < split, else csn. 112 columns: two TMEM loads per wait; 80
+// columns: all three loads, then one wait.
 template <int HALF>
 __device__ __forceinline__ void promote_odd(float (&acc)[HALF], uint32_t taddr, int h, float cs,
                                             float csn, int split) {
-    static_assert(HALF == 112, "112 columns per warp");
+    static_assert(HALF == 112 || HALF == 80, "112 or 80 columns per warp");
     const int b = 16 * h, o16 = (HALF - 16) * (1 - h);
     uint32_t r0[32], r1[32];
-    tmem_ld32(taddr + b, r0);
-    tmem_ld32(taddr + b + 32, r1);
-    tmem_wait_ld64(r0, r1);
-    fma_cols<0, 32>(acc, r0, b < split ? cs : csn);
-    fma_cols<32, 32>(acc, r1, b + 32 < split ? cs : csn);
-    uint32_t r2[32], r3[16];
-    tmem_ld32(taddr + b + 64, r2);
-    tmem_ld16(taddr + o16, r3);
-    tmem_wait_ld48(r2, r3);
-    fma_cols<64, 32>(acc, r2, b + 64 < split ? cs : csn);
-    fma_cols<HALF - 16, 16>(acc, r3, o16 < split ? cs : csn);
+    if constexpr (HALF == 112) {
+        tmem_ld32(taddr + b, r0);
+        tmem_ld32(taddr + b + 32, r1);
+        tmem_wait_ld64(r0, r1);
+        fma_cols<0, 32>(acc, r0, b < split ? cs : csn);
+        fma_cols<32, 32>(acc, r1, b + 32 < split ? cs : csn);
+        uint32_t r2[32], r3[16];
+        tmem_ld32(taddr + b + 64, r2);
+        tmem_ld16(taddr + o16, r3);
+        tmem_wait_ld48(r2, r3);
+        fma_cols<64, 32>(acc, r2, b + 64 < split ? cs : csn);
+        fma_cols<HALF - 16, 16>(acc, r3, o16 < split ? cs : csn);
+    } else {
+        uint32_t r3[16];
+        tmem_ld32(taddr + b, r0);
+        tmem_ld32(taddr + b + 32, r1);
+        tmem_ld16(taddr + o16, r3);
+        tmem_wait_ld64(r0, r1);
+        reg_order16(r3);  // the wait above covers r3's load too
+        fma_cols<0, 32>(acc, r0, b < split ? cs : csn);
+        fma_cols<32, 32>(acc, r1, b + 32 < split ? cs : csn);
+        fma_cols<HALF - 16, 16>(acc, r3, o16 < split ? cs : csn);
+    }
 }
 
 // Column of this warp's tile slice that acc[i] holds: i itself, except for
-// 112-column warps (224-wide tiles), whose chunk order puts warp columns
-// 16 h .. 16 h + 95 in acc[0, 96) and the remaining 16 columns in acc[96, 112).
+// 112- and 80-column warps (224- and 160-wide tiles), whose chunk order puts
+// warp columns 16 h .. 16 h + HALF - 17 in acc[0, HALF - 16) and the
+// remaining 16 columns in acc[HALF - 16, HALF).
 template <int HALF>
 __device__ __forceinline__ int acc_col(int i, int h) {
     if constexpr (HALF % 32 == 0) {
@@ -757,8 +775,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             // For BN = 128 and 256 this warp's columns lie in one 128-column
             // block (n0 % BN == 0), so each K block needs one scale product
-            // sa[m][kb] * sb[nb][kb]. A 224-wide tile starts at a multiple of 32
-            // and a warp's 112 columns touch at most two blocks: the first
+            // sa[m][kb] * sb[nb][kb]. A 160- or 224-wide tile starts at a multiple
+            // of 32 and a warp's 80 or 112 columns touch at most two blocks: the first
             // `split` columns use block rel_nb, the rest block rel_nb + 1.
             const int wcol = (tile.n0 & 127) + h * L::HALF;  // from the tile's first block
             const int rel_nb = wcol >> 7;
@@ -795,7 +813,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float b_s = j == 0 ? sb4.x : j == 1 ? sb4.y : j == 2 ? sb4.z : sb4.w;
                 const float cs = a_s * b_s;
                 const float b_sn = j == 0 ? sb4n.x : j == 1 ? sb4n.y : j == 2 ? sb4n.z : sb4n.w;
-                const float csn = a_s * b_sn;  // 224-wide tiles: the warp's second block
+                const float csn = a_s * b_sn;  // 160/224-wide tiles: the warp's second block
 
                 if (!warp_wait<PAIR>(bar(L::TFULL + abuf), aphase, abort_flag, limit)) {
                     ok = false;

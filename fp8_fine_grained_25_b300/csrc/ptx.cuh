@@ -506,6 +506,16 @@ __device__ __forceinline__ void tmem_wait_ld48(uint32_t (&a)[32], uint32_t (&b)[
                  : "memory");
 }
 
+// No instruction: orders the use of a 16-register TMEM load group after a
+// preceding tcgen05.wait::ld issued for other registers (the compiler sees
+// the group rewritten here, so it cannot read the registers earlier).
+__device__ __forceinline__ void reg_order16(uint32_t (&r)[16]) {
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+                 :
+                 : "memory");
+}
+
 // Register reallocation between warpgroups (all warps of a warpgroup
 // execute the same one).
 template <int N>

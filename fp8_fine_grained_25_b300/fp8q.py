@@ -460,8 +460,9 @@ def fp8q_set_wait_timeout_ns(ns: int) -> None:
 
 
 def fp8q_set_gemm_tile_n(bn: int) -> None:
-    """Force the dense GEMM's output-tile width (128, 224 or 256; 0 = automatic;
-    224 applies to the block-scaled GEMM, the weight-gradient GEMM runs 256)."""
+    """Force the dense GEMM's output-tile width (128, 160, 224 or 256; 0 =
+    automatic; 160 and 224 apply to the block-scaled GEMM, the weight-gradient
+    GEMM runs 256; 160 to pair tiles only, without split K)."""
     _check(lib.fp8q_set_gemm_tile_n(int(bn)), "fp8q_set_gemm_tile_n")
 
 

@@ -342,10 +342,12 @@ FP8Q_API int fp8q_get_device_status(cudaStream_t stream, uint32_t* status_out, i
 FP8Q_API void fp8q_set_wait_timeout_ns(uint64_t ns);
 
 /*
- * Output-tile width of fp8_block_gemm and fp8_wgrad_gemm: 128, 224 or 256
- * columns, or 0 (the default) to let the library pick per shape. 224 applies
- * to fp8_block_gemm only (fp8_wgrad_gemm then runs 256 wide). Affects speed
- * only, never results. Returns FP8Q_ERR_UNSUPPORTED for other values.
+ * Output-tile width of fp8_block_gemm and fp8_wgrad_gemm: 128, 160, 224 or
+ * 256 columns, or 0 (the default) to let the library pick per shape. 160 and
+ * 224 apply to fp8_block_gemm only (fp8_wgrad_gemm then runs 256 wide); 160
+ * applies to 2-CTA pair tiles only (M > 128) and is never split over K (a
+ * call that cannot use it runs at the width the library picks). Affects
+ * speed only, never results. Returns FP8Q_ERR_UNSUPPORTED for other values.
  */
 FP8Q_API int fp8q_set_gemm_tile_n(int bn);
 

@@ -208,9 +208,9 @@ def test_ue8m0_quantizer_argument_checks(lib):
 def test_tile_width_setter(lib):
     # the setters only record a process-wide choice; no device is touched
     OK, UNSUPPORTED = 0, 7
-    for bn in (0, 128, 224, 256):
+    for bn in (0, 128, 160, 224, 256):
         assert lib.fp8q_set_gemm_tile_n(bn) == OK, bn
-    for bn in (64, 160, 192, 512, -1):
+    for bn in (64, 192, 512, -1):
         assert lib.fp8q_set_gemm_tile_n(bn) == UNSUPPORTED, bn
     assert lib.fp8q_set_gemm_tile_n(0) == OK
 

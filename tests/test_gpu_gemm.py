@@ -1,7 +1,7 @@
 """GPU block-scaled GEMM vs the CPU oracle, within
 |C - C_oracle| <= 1 bf16 ulp + 1e-5 * sum_k |a_k b_k|, on ragged small
 shapes (full output), random codes with wide dynamic range, every tile
-width (128, 224, 256), and sampled outputs of the full-size workloads."""
+width (128, 160, 224, 256), and sampled outputs of the full-size workloads."""
 import numpy as np
 import pytest
 import torch
@@ -52,7 +52,7 @@ SHAPES = [(128, 256, 512), (1, 8, 16), (300, 520, 400), (129, 264, 144), (257, 5
           (640, 1536, 1024), (1000, 2056, 256), (384, 384, 2048)]
 
 
-@pytest.mark.parametrize("bn", [0, 128, 224, 256])
+@pytest.mark.parametrize("bn", [0, 128, 160, 224, 256])
 @pytest.mark.parametrize("M,N,K", SHAPES)
 def test_gemm_random_codes_full_output(q, M, N, K, bn):
     q.fp8q_set_gemm_tile_n(bn)
@@ -69,7 +69,8 @@ def test_gemm_random_codes_full_output(q, M, N, K, bn):
 # staging buffer of a skipped box must not be handed to the next store while
 # an earlier store still reads it. Repeated, since a race shows up by chance.
 @pytest.mark.parametrize("M,N,K,bn", [(300, 376, 512, 224), (1000, 2176, 256, 224),
-                                      (129, 600, 384, 224)])
+                                      (129, 600, 384, 224), (300, 376, 512, 160),
+                                      (129, 600, 384, 160)])
 def test_gemm_ragged_last_tile_stores(q, M, N, K, bn):
     qa, sa, qb, sb = _random_operands(M, N, K, 3 * M + N + K)
     c32, S = oracle.gemm(qa, sa, qb, sb)
@@ -86,26 +87,29 @@ def test_gemm_ragged_last_tile_stores(q, M, N, K, bn):
 def test_gemm_tile_widths_agree_bitwise(q, pairs):
     # Every tile width runs the same arithmetic per output element. N = 776
     # puts 224-wide tiles at column offsets 0, 96 and 64 of a 128-column
-    # scale block, and ends in a partial tile.
+    # scale block (160-wide: 0, 32, 64, 96), and ends in a partial tile.
+    # 160-wide tiles are pair tiles only: without pairs the call runs at
+    # the automatic width.
     qa, sa, qb, sb = _random_operands(333, 776, 1024, 5)
     q.fp8q_set_gemm_pairs(pairs)
     try:
         out = {}
-        for bn in (128, 224, 256):
+        for bn in (128, 160, 224, 256):
             q.fp8q_set_gemm_tile_n(bn)
             out[bn] = _run(q, qa, sa, qb, sb).clone()
     finally:
         q.fp8q_set_gemm_tile_n(0)
         q.fp8q_set_gemm_pairs(True)
-    for bn in (128, 224):
+    for bn in (128, 160, 224):
         assert torch.equal(out[bn].view(torch.int16), out[256].view(torch.int16)), bn
 
 
-@pytest.mark.parametrize("bn", [128, 224, 256])
+@pytest.mark.parametrize("bn", [128, 160, 224, 256])
 def test_gemm_several_tiles_per_cluster(q, bn):
     """4096 x 2048 outputs in 256-row pair tiles are 2-4 tiles per 2-CTA
     cluster, so each CTA stages and stores several output tiles through the
-    same shared memory (224 wide: a 32-column last tile); the full output is
+    same shared memory (224 wide: a 32-column last tile; 160 wide: 128
+    columns, and three TMEM accumulators in turn); the full output is
     checked on two runs in a row."""
     qa, sa, qb, sb = _random_operands(4096, 2048, 256, 11 + bn)
     c32, S = oracle.gemm(qa, sa, qb, sb)
