@@ -6,15 +6,6 @@
 
 namespace fp8q {
 
-int gemm_stages(int bn) {
-    switch (bn) {
-        case 128: return Layout<128, false, false>::STAGES;
-        case 224: return Layout<224, false, false>::STAGES;
-        case 256: return Layout<256, false, false>::STAGES;
-        default: return 0;
-    }
-}
-
 int gemm_c_box_cols(int bn, bool pair) {
     switch (bn) {
         case 128: return pair ? Layout<128, false, true>::EPI_BOX_COLS : Layout<128, false, false>::EPI_BOX_COLS;

@@ -48,7 +48,6 @@ struct GemmLaunch {
 };
 
 cudaError_t launch_gemm(const GemmLaunch& g);
-int gemm_stages(int bn);
 // Columns of the TMA-store box of C the kernel writes through (the tensor
 // map's box width: 64 with a 128-byte swizzle, 32 with a 64-byte swizzle, or
 // 16 with a 32-byte swizzle), for one-CTA or pair tiles.
