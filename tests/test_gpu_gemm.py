@@ -48,8 +48,11 @@ def _run(q, qa, sa, qb, sb, guard=True):
     return C
 
 
+# (300, 8, 64) and (257, 24, 128): pair tiles whose output is narrower than one
+# store box (every width clips its first box and skips the rest) over less
+# than one K block
 SHAPES = [(128, 256, 512), (1, 8, 16), (300, 520, 400), (129, 264, 144), (257, 576, 7168),
-          (640, 1536, 1024), (1000, 2056, 256), (384, 384, 2048)]
+          (640, 1536, 1024), (1000, 2056, 256), (384, 384, 2048), (300, 8, 64), (257, 24, 128)]
 
 
 @pytest.mark.parametrize("bn", [0, 128, 160, 224, 256])
