@@ -125,6 +125,34 @@ def test_split_k_small_workspace_falls_back(q):
     assert_gemm_ok(to_f32(C2), c32, S, "two ranges in a small workspace")
 
 
+def test_split_k_with_160_wide_tiles_runs_unsplit(q):
+    """160-wide pair tiles have no split-K form: with that width forced, the
+    workspace query says 0 bytes and fp8_block_gemm_ws gives the bits of
+    fp8_block_gemm at that width; without pairs the call runs at another
+    width and splits again."""
+    host_ops = _random_operands(257, 576, 4096, 21)
+    ops = _dev(*host_ops)
+    ws = torch.randint(0, 256, (32 << 20,), dtype=torch.uint8, device=DEV)
+    q.fp8q_set_gemm_tile_n(160)
+    q.fp8q_set_gemm_splits(3)
+    try:
+        assert q.fp8_block_gemm_workspace_size(257, 576, 4096) == 0
+        C = _run_ws(q, ops, ws).clone()
+        plain = q.fp8_block_gemm(*ops)
+        torch.cuda.synchronize()
+        assert torch.equal(C.view(torch.int16), plain.view(torch.int16))
+        q.fp8q_set_gemm_pairs(False)
+        assert q.fp8_block_gemm_workspace_size(257, 576, 4096) > 0
+        C1 = _run_ws(q, ops, ws)
+    finally:
+        q.fp8q_set_gemm_tile_n(0)
+        q.fp8q_set_gemm_splits(0)
+        q.fp8q_set_gemm_pairs(True)
+    c32, S = oracle.gemm(*host_ops)
+    assert_gemm_ok(to_f32(C), c32, S, "160 wide, split request ignored")
+    assert_gemm_ok(to_f32(C1), c32, S, "one-CTA tiles, three ranges")
+
+
 def _sampled_ws(q, A, W, name, n_rows=96, n_cols=48, seed=0):
     M, K = A.shape
     N = W.shape[0]
